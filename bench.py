@@ -1,0 +1,340 @@
+#!/usr/bin/env python3
+"""Throughput of the tensor-sliced MLP block forward+backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mtnlg] [--impl ours|reference]
+
+One step = every micro-batch of the workload through mlp_fwd + mlp_bwd (all
+slices in turn, partial sums reduced on the device, fp32 weight gradients
+accumulated).  Prints one JSON line (rank 0).  Under torchrun each rank runs its
+own replica of the workload (weak scaling, no collective on the data path).
+
+Workload default: the MT-NLG-layer-shaped block, 2048 tokens, h 20480, ffn 81920,
+t = 8 slices, one micro-batch; every input is seeded synthetic data.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLP block fwd+bwd TFLOP/s and % of GB300 dense-BF16 peak (1 GPU)"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"bf16_burst": d["bf16_tflops"], "bf16_sustained": d["bf16_tflops_sustained"],
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = max(mx, float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle sample
+def oracle_sample(wl, weights_host, n_tokens: int, slice_index: int = 0):
+    """Times the oracle (float64, host cores) on a bounded sample of the workload:
+    ``n_tokens`` tokens through one slice (A_i columns, B_i rows) forward+backward.
+    Returns (seconds, algorithmic flops of the sample)."""
+    import numpy as np
+    from oracle import mlp_oracle as orc
+    from transformer_lm_megatron_gb300 import inputs as gin
+
+    A, a, B, b = weights_host
+    f = wl.f
+    cols = slice(slice_index * f, (slice_index + 1) * f)
+    A_i = orc.bf16_to_f64(gin.bf16_bits(A[:, cols]))
+    a_i = orc.bf16_to_f64(gin.bf16_bits(a[cols]))
+    B_i = orc.bf16_to_f64(gin.bf16_bits(B[cols, :]))
+    b64 = orc.bf16_to_f64(gin.bf16_bits(b))
+    X, dO = gin.make_microbatch(n_tokens, wl.h, 0)
+    X64 = orc.bf16_to_f64(gin.bf16_bits(X))
+    dO64 = orc.bf16_to_f64(gin.bf16_bits(dO))
+    t0 = time.perf_counter()
+    fw = orc.mlp_fwd(X64, A_i, a_i, B_i, b64, 1, wl.p, wl.seed, mirror=True)
+    orc.mlp_bwd(dO64, X64, A_i, B_i, fw["U"], fw["Y"], fw["keep"], 1, wl.p, mirror=True)
+    dt = time.perf_counter() - t0
+    return dt, 12 * n_tokens * wl.h * f
+
+
+def _cpu_cores():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def _sample_weights_host(wl, device):
+    """Slice-0 weights of the workload, drawn on ``device`` with the seeded generator, on the host."""
+    from transformer_lm_megatron_gb300 import inputs as gin
+    w = gin.make_weights(wl.h, wl.ffn, device=device)
+    return tuple(x.cpu() for x in w)
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, wl, rank, world):
+    """The CPU oracle timed on the host cores: each step is a bounded sample."""
+    if rank != 0:
+        return
+    import numpy as np  # noqa: F401
+    from transformer_lm_megatron_gb300 import inputs as gin
+    w = gin.make_weights(wl.h, wl.ffn, device="cpu") if wl.h * wl.ffn <= 64 * 2**20 else None
+    if w is None:
+        import torch
+        w = _sample_weights_host(wl, "cuda" if torch.cuda.is_available() else "cpu")
+    n_tok = args.cpu_tokens
+    for _ in range(args.warmup):
+        oracle_sample(wl, w, n_tok)
+    times, flops = [], 0
+    for _ in range(args.steps):
+        dt, fl = oracle_sample(wl, w, n_tok)
+        times.append(dt)
+        flops = fl
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = f"{n_tok} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, float64, per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "tokens": wl.tokens, "h": wl.h, "ffn": wl.ffn, "t": wl.t, "k": wl.k},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, wl, rank, world, dist):
+    import torch
+    from transformer_lm_megatron_gb300 import build as gb_build
+    from transformer_lm_megatron_gb300 import inputs as gin
+    from transformer_lm_megatron_gb300 import mlp
+
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    gb_build.build()
+    mlp.load()
+
+    weights = gin.make_weights(wl.h, wl.ffn, device=dev)
+    mbs = [gin.make_microbatch(wl.tokens, wl.h, j, device=dev) for j in range(wl.k)]
+    buf = mlp.BlockBuffers(wl.tokens, wl.h, wl.ffn, wl.t, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for j, (X, dO) in enumerate(mbs):
+            mlp.block_step(wl, weights, X, dO, buf, token_offset=j * wl.tokens, slice_mode=args.slice_mode,
+                           stream=stream)
+
+    mlp.grad_accum_reset(wl.h, wl.ffn, buf.dA, buf.da, buf.dB, buf.db, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
+        raise RuntimeError(mlp.last_error())
+
+    # ---- timed region (device time, CUDA events on the launching stream)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    trace = mlp.Trace(capacity=args.steps * 80 * wl.k) if args.trace else None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    n_launch0 = mlp.mlp_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    if trace:
+        trace.start()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if trace:
+        trace.stop()
+    n_launch = mlp.mlp_launch_count() - n_launch0
+    if dist is not None:
+        dist.barrier()
+    clock_info = clocks.stop() if clocks else None
+    ms = ev0.elapsed_time(ev1)
+    if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
+        raise RuntimeError(mlp.last_error())
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    flops_step = wl.flops_total()
+    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if not args.no_e2e:
+        hX = [X.cpu().pin_memory() for X, _ in mbs]
+        hdO = [dO.cpu().pin_memory() for _, dO in mbs]
+        hO = [torch.empty_like(X, device="cpu").pin_memory() for X, _ in mbs]
+        hdX = [torch.empty_like(X, device="cpu").pin_memory() for X, _ in mbs]
+        dX_in = [torch.empty_like(X) for X, _ in mbs]
+        ddO_in = [torch.empty_like(dO) for _, dO in mbs]
+
+        def e2e_step():
+            for j in range(wl.k):
+                dX_in[j].copy_(hX[j], non_blocking=True)
+                ddO_in[j].copy_(hdO[j], non_blocking=True)
+                mlp.block_step(wl, weights, dX_in[j], ddO_in[j], buf, token_offset=j * wl.tokens,
+                               slice_mode=args.slice_mode, stream=stream)
+                hO[j].copy_(buf.O, non_blocking=True)
+                hdX[j].copy_(buf.dX, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ems = e0.elapsed_time(e1)
+        if dist is not None:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        act = wl.tokens * wl.h * 2 * wl.k
+        e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": 2 * act, "d2h_bytes_per_step": 2 * act, "ms_per_step": ems / args.steps}
+
+    if rank != 0:
+        return
+    peaks = _peaks()
+    roofline = None
+    if trace:
+        roofline = trace.roofline(peaks, args.steps)
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        w_host = tuple(x.cpu() for x in weights)
+        dt, fl = oracle_sample(wl, w_host, args.cpu_tokens)
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
+               "sample": f"{args.cpu_tokens} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, "
+                         f"float64 numpy, {dt:.1f} s"}
+    burst = peaks["bf16_burst"]
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "pct_of_peak": 100.0 * value / (world * burst),
+        "peak_tflops": {"value": burst, "kind": f"bf16 dense burst, {peaks['source']}"},
+        "config": {"workload": wl.name, "tokens": wl.tokens, "h": wl.h, "ffn": wl.ffn, "t": wl.t,
+                   "micro_batches": wl.k, "dropout": wl.p, "slice_calls": args.slice_mode,
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, all slices on-device",
+                   "l2": "inputs larger than L2 (bf16 weights %.1f GB, fp32 gradients %.1f GB)"
+                         % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9),
+                   "grad_accum_reset": "outside the timed region"},
+        "gpu_launches": n_launch,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clock_info,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="mtnlg")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--slice-mode", default="all", choices=["all", "each"])
+    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-trace", dest="trace", action="store_false")
+    args = ap.parse_args()
+
+    from transformer_lm_megatron_gb300 import inputs as gin
+    wl = gin.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    run_ours(args, wl, rank, world, dist)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

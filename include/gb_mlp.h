@@ -1,0 +1,175 @@
+/*
+ * gb_mlp.h - C ABI of the tensor-sliced transformer MLP block (forward, backward,
+ * fp32 gradient accumulation) on one GB300 GPU (sm_103a).
+ *
+ * The operation (Megatron tensor-parallel MLP, "STRONGHOLD: Fast and Affordable
+ * Billion-scale Deep Learning Model Training", slides items 7-8; gradient
+ * accumulation over micro-batches, "Using DeepSpeed and Megatron to Train
+ * Megatron-Turing NLG 530B", Key points):
+ *
+ *   A [h, ffn] is split column-wise into t slices A_i = A[:, i*f:(i+1)*f], f = ffn/t
+ *   B [ffn, h] is split row-wise    into t slices B_i = B[i*f:(i+1)*f, :]
+ *   forward   U_i = X A_i + a_i,  Y_i = GeLU(U_i),  Z = sum_i Y_i B_i   (operator g)
+ *             O   = R + dropout(Z + b)
+ *   backward  dZ = dO * m / (1-p),  db += sum_tok dZ
+ *             dU_i = (dZ B_i^T) * GeLU'(U_i),  da_i += sum_tok dU_i
+ *             dB_i += Y_i^T dZ,  dA_i += X^T dU_i
+ *             dX = [dO +] sum_i dU_i A_i^T                               (operator f)
+ *
+ * Every slice runs on this GPU; the sums over slices that the pages perform with
+ * all-reduces across GPUs are on-device fp32 reductions here.
+ *
+ * GeLU is the tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).  Dropout
+ * is inverted dropout: element e = (token_offset + token) * h + column of the
+ * [tokens, h] output is kept iff (SplitMix64(seed, e) >> 32) >= round(p * 2^32),
+ * where SplitMix64(seed, e) is output number e of a SplitMix64 stream seeded with
+ * `seed` (Steele, Lea & Flood, OOPSLA 2014), and kept values are scaled by
+ * 1/(1-p).  The mask does not depend on t, the slice, or any value.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are row-major and contiguous; mlp_bf16 is the raw bit pattern of a
+ *     bfloat16.  Shapes: X, R, O, dO, dX, dZ [tokens, h]; U, Y, dU [tokens, ffn];
+ *     A [h, ffn]; a [ffn]; B [ffn, h]; b [h]; dA [h, ffn]; da [ffn]; dB [ffn, h];
+ *     db [h]; Zacc, dXacc [tokens, h] fp32.
+ *   - All pointers are DEVICE pointers owned by the caller, 16-byte aligned.  The
+ *     library allocates no device memory; it keeps only a 2-word status word.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and runs asynchronously.  A nonzero return means nothing was enqueued,
+ *     except MLP_ECUDA, which reports a failed launch (later launches of the same
+ *     call are not attempted).  mlp_last_error() describes the failure.
+ *   - Constraints: h > 0, h % 8 == 0; ffn % t == 0, f = ffn/t, f % 8 == 0;
+ *     0 < tokens < 2^31; 0 <= p < 1; -1 <= slice < t.
+ *   - A kernel that detects a broken pipeline (a bounded wait that ran out)
+ *     records MLP_ETIMEOUT in the device status word and returns;
+ *     mlp_sync_status() reports it.
+ */
+#ifndef GB_MLP_H
+#define GB_MLP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mlp_bf16; /* raw bfloat16 bits */
+
+enum {
+  MLP_OK = 0,
+  MLP_EINVAL = -1,       /* a size, count or probability out of range, or a NULL pointer */
+  MLP_EALIGN = -2,       /* a pointer not 16-byte aligned */
+  MLP_EUNSUPPORTED = -3, /* no sm_103a device, or a shape the kernels do not take */
+  MLP_ECUDA = -4,        /* a CUDA call or launch failed */
+  MLP_ETIMEOUT = -5      /* a kernel gave up on a bounded wait (device status word) */
+};
+
+/*
+ * mlp_fwd - forward of one micro-batch (STRONGHOLD slides, items 7-8).
+ *
+ *   slice == -1: all t slices in turn inside this call.
+ *   slice == i : slice i only.  Calls must come in order i = 0 .. t-1 on one
+ *                stream; slice 0 overwrites Zacc, slices 0 .. t-2 accumulate
+ *                into it, and slice t-1 writes O.
+ *   X      [tokens, h]   input activations.
+ *   A, a   [h, ffn], [ffn]   first weight and bias (slice i = columns i*f ..).
+ *   B, b   [ffn, h], [h]     second weight and bias (slice i = rows i*f ..).
+ *   R      [tokens, h]   residual; NULL means R = X.
+ *   U, Y   [tokens, ffn] outputs: pre-activation and GeLU output (bf16), kept
+ *                        for the backward; slice i writes columns i*f .. .
+ *   Zacc   [tokens, h] fp32 workspace for the sum over slices; may be NULL
+ *                        when t == 1.
+ *   O      [tokens, h]   output, written by the last slice.
+ * Returns MLP_OK or an error code.
+ */
+int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,
+            const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B, const mlp_bf16* b,
+            const mlp_bf16* R, mlp_bf16* U, mlp_bf16* Y, float* Zacc, mlp_bf16* O, void* stream);
+
+/*
+ * mlp_bwd - backward of one micro-batch; weight and bias gradients ACCUMULATE
+ * (+=) into the fp32 dA, da, dB, db (gradient accumulation over micro-batches).
+ *
+ *   slice == -1 or slice == i as for mlp_fwd (order 0 .. t-1).  The call with
+ *   slice 0 (or -1) computes dZ and db; the call with slice t-1 writes dX.
+ *   residual_grad  1: dX = dO + sum_i dU_i A_i^T (the residual R was X);
+ *                  0: dX = sum_i dU_i A_i^T.
+ *   dO     [tokens, h]  upstream gradient of O.
+ *   X, A, B           as passed to mlp_fwd; U, Y as written by mlp_fwd.
+ *   dZ     [tokens, h]  workspace/output: gradient after dropout (bf16).
+ *   dU     [tokens, ffn] workspace/output: gradient of the pre-activation (bf16).
+ *   dXacc  [tokens, h] fp32 workspace for the sum over slices; may be NULL when
+ *                        t == 1.
+ *   dX     [tokens, h]  output (overwritten).
+ *   dA, da, dB, db    fp32 gradient accumulators (+=).
+ * Returns MLP_OK or an error code.
+ */
+int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,
+            int residual_grad, const mlp_bf16* dO, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
+            const mlp_bf16* U, const mlp_bf16* Y, mlp_bf16* dZ, mlp_bf16* dU, float* dXacc, mlp_bf16* dX,
+            float* dA, float* da, float* dB, float* db, void* stream);
+
+/*
+ * grad_accum_reset - zero the fp32 gradient accumulators dA [h, ffn], da [ffn],
+ * dB [ffn, h], db [h] before the first micro-batch of a step (gradient
+ * accumulation, MT-NLG summary page, Key points).  Returns MLP_OK or an error.
+ */
+int grad_accum_reset(int h, int ffn, float* dA, float* da, float* dB, float* db, void* stream);
+
+/*
+ * mlp_sync_status - synchronise `stream`, then return and clear the device status
+ * word: MLP_OK, or MLP_ETIMEOUT if a kernel gave up on a bounded wait since the
+ * last call (mlp_last_error() then names the wait), or MLP_ECUDA.
+ */
+int mlp_sync_status(void* stream);
+
+/* mlp_last_error - thread-local description of the last nonzero return. */
+const char* mlp_last_error(void);
+
+/*
+ * mlp_dropout_mask - the keep mask the forward and backward use, one byte per
+ * element of the [tokens, h] output (1 = kept), written to device memory m.
+ * For tests and inspection; the block itself never materialises the mask.
+ */
+int mlp_dropout_mask(int h, int64_t tokens, float p, uint64_t seed, uint64_t token_offset, uint8_t* m,
+                     void* stream);
+
+/*
+ * mlp_gelu_probe - y[i] = GeLU(x[i]), dy[i] = GeLU'(x[i]) for n fp32 device
+ * values, with the same device functions the GEMM epilogues use.  For tests.
+ */
+int mlp_gelu_probe(const float* x, int64_t n, float* y, float* dy, void* stream);
+
+/*
+ * mlp_wait_timeout_probe - launch one kernel that waits on a barrier nothing
+ * arrives on, giving up after limit_ns nanoseconds, so that the next
+ * mlp_sync_status() returns MLP_ETIMEOUT.  Tests the error path of bounded waits
+ * without faulting or hanging the GPU.  limit_ns must be <= 10^9.
+ */
+int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream);
+
+/* mlp_launch_count - number of kernels this library has launched in this process. */
+uint64_t mlp_launch_count(void);
+
+/*
+ * mlp_trace_begin - from now on, bracket every kernel this library launches with
+ * a pair of CUDA events on the launch stream, for at most `capacity` launches
+ * (later launches are not traced).  The events are created here (host-side
+ * resources only).  Returns MLP_OK, or MLP_EINVAL if a trace is already running.
+ */
+int mlp_trace_begin(int capacity);
+
+/*
+ * mlp_trace_end - stop tracing, wait for the traced launches and report up to
+ * max_entries of them in launch order: kinds[i] (0..5 = the GEMMs F1, F2, B2, B3,
+ * B4, B5 of the forward/backward; 10 = dropout backward + db; 11 = column sum
+ * for da; 12 = accumulator reset), mnk[3i..3i+2] = the launch's M, N, K (GEMMs)
+ * or rows, columns, 0, and ms[i] = its device time in milliseconds.  Any output
+ * pointer may be NULL.  Returns the number of entries written, or an error code.
+ */
+int mlp_trace_end(int max_entries, int* kinds, int64_t* mnk, float* ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GB_MLP_H */

@@ -1,0 +1,168 @@
+"""GPU parity of the tensor-sliced MLP block against the CPU oracle, through the C ABI.
+
+Bars: the dropout mask bit-exact; bf16 activations and gradients within
+max|gpu - oracle| / max|oracle| <= 1e-2 of both oracle modes; fp32 accumulated
+weight and bias gradients within 1e-3 of the oracle's bf16-mirroring mode.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mlp_oracle as orc
+from transformer_lm_megatron_gb300 import build as gb_build
+from transformer_lm_megatron_gb300 import mlp
+
+from gpu_harness import (BF16_TOL, F32_TOL, Shape, compare_full, make_case, rel_err, run_gpu, run_oracle, to_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    gb_build.build()
+    mlp.load()
+    torch.cuda.synchronize()
+
+
+def test_gelu_device_functions_exhaustive_bf16():
+    """Every finite bf16 value as a pre-activation: GeLU and GeLU' against fp64."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x64 = orc.bf16_to_f64(bits)
+    x64 = x64[np.isfinite(x64)]
+    x = torch.from_numpy(x64.astype(np.float32)).cuda()
+    y = torch.empty_like(x)
+    dy = torch.empty_like(x)
+    mlp.mlp_gelu_probe(x, y, dy)
+    torch.cuda.synchronize()
+    ref_y = orc.gelu(x64)
+    ref_dy = orc.gelu_prime(x64)
+    gy = y.cpu().numpy().astype(np.float64)
+    gdy = dy.cpu().numpy().astype(np.float64)
+    # fp32 evaluation: error relative to max(|value|, 1) stays at a few fp32 ulps
+    ey = np.abs(gy - ref_y) / np.maximum(np.abs(ref_y), 1.0)
+    edy = np.abs(gdy - ref_dy) / np.maximum(np.abs(ref_dy), 1.0)
+    assert np.all(np.isfinite(gy)) and np.all(np.isfinite(gdy))
+    assert ey.max() < 2e-6, ey.max()
+    assert edy.max() < 2e-6, edy.max()
+
+
+@pytest.mark.parametrize("h,tokens,p,seed,off", [(64, 100, 0.1, 1234, 0), (768, 33, 0.5, 7, 4096),
+                                                   (20480, 8, 0.1, 1234, 2**40), (136, 5, 0.0, 1, 3)])
+def test_dropout_mask_bit_exact(h, tokens, p, seed, off):
+    m = torch.empty(tokens, h, dtype=torch.uint8, device="cuda")
+    mlp.mlp_dropout_mask(h, tokens, p, seed, off, m)
+    ref = orc.dropout_keep(tokens, h, p, seed, off)
+    np.testing.assert_array_equal(m.cpu().numpy().astype(bool), ref)
+
+
+TINY = Shape(tokens=256, h=256, ffn=1024, t=2, k=2)
+
+
+def test_tiny_workload_full_parity():
+    """The tiny workload (256 tokens, h 256, ffn 1024, t 2, two micro-batches)."""
+    w_dev, mbs_dev, w64, mbs64 = make_case(TINY)
+    g_outs, g_grads = run_gpu(TINY, w_dev, mbs_dev, keep_all=True)
+    for mirror in (True, False):
+        r_outs, r_grads = run_oracle(TINY, w64, mbs64, mirror=mirror, keep_all=True)
+        compare_full(TINY, g_outs, g_grads, r_outs, r_grads, check_grads=mirror, label=f"mirror={mirror}")
+        # the mask decides exactly: dropped outputs equal the residual, dropped dZ are zero
+        for j in range(TINY.k):
+            keep = orc.dropout_keep(TINY.tokens, TINY.h, TINY.p, TINY.seed, j * TINY.tokens)
+            O = to_f64(g_outs[j]["O"])
+            X = mbs64[j][0]
+            np.testing.assert_array_equal(O[~keep], X[~keep])
+            assert np.all(to_f64(g_outs[j]["dZ"])[~keep] == 0)
+
+
+@pytest.mark.parametrize("tokens,h,ffn,t", [
+    (200, 136, 656, 2),     # ragged M, N and K tails (none a multiple of the 128/256/64 tiles)
+    (1, 64, 128, 1),        # a single token
+    (130, 8, 64, 4),        # h = 8: one partial k-block, f = 16
+    (384, 320, 1280, 1),    # several M tiles, N tail of 64
+])
+def test_ragged_shapes_full_parity(tokens, h, ffn, t):
+    s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2, p=0.1)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    g_outs, g_grads = run_gpu(s, w_dev, mbs_dev)
+    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
+    compare_full(s, g_outs, g_grads, r_outs, r_grads)
+
+
+def test_slice_invariance_and_per_slice_calls():
+    """t = 1, 2, 4, 8 agree within tolerance with identical dropped positions; one
+    call per slice gives bit-identical results to the all-slices call."""
+    base = None
+    for t in (1, 2, 4, 8):
+        s = Shape(tokens=256, h=256, ffn=2048, t=t, k=1)
+        w_dev, mbs_dev, w64, mbs64 = make_case(s)
+        outs, grads = run_gpu(s, w_dev, mbs_dev, slice_mode="all")
+        if t > 1:
+            outs_each, grads_each = run_gpu(s, w_dev, mbs_dev, slice_mode="each")
+            for k in outs[0]:
+                assert torch.equal(outs[0][k], outs_each[0][k]), k
+            for k in grads:
+                assert torch.equal(grads[k], grads_each[k]), k
+        if base is None:
+            base = (outs, grads)
+            continue
+        for k in ("O", "dX", "U", "Y", "dU", "dZ"):
+            assert rel_err(to_f64(outs[0][k]), to_f64(base[0][0][k])) <= BF16_TOL, (t, k)
+        for k in grads:
+            assert rel_err(to_f64(grads[k]), to_f64(base[1][k])) <= F32_TOL, (t, k)
+        O = to_f64(outs[0]["O"])
+        X = mbs64[0][0]
+        keep = orc.dropout_keep(s.tokens, s.h, s.p, s.seed, 0)
+        np.testing.assert_array_equal(O[~keep], X[~keep])
+
+
+def test_exact_invariants():
+    """Power-of-two scaling of dO scales every gradient exactly; zero second layer
+    gives O == X exactly; reset + one micro-batch equals a fresh run bit for bit."""
+    s = Shape(tokens=192, h=128, ffn=512, t=2, k=1)
+    w_dev, mbs_dev, _, _ = make_case(s)
+    outs1, g1 = run_gpu(s, w_dev, mbs_dev)
+    X, dO = mbs_dev[0]
+    outs2, g2 = run_gpu(s, w_dev, [(X, dO * 2)])
+    for k in g1:
+        assert torch.equal(g2[k], g1[k] * 2), k
+    assert torch.equal(outs2[0]["dX"].float(), outs1[0]["dX"].float() * 2)
+    # checkpoint/restore of the accumulators: accumulate, copy, continue == uninterrupted
+    buf = mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t)
+    run_gpu(s, w_dev, mbs_dev, buf=buf)
+    saved = {k: getattr(buf, k).clone() for k in ("dA", "da", "dB", "db")}
+    _, g_cont = run_gpu(s, w_dev, mbs_dev, buf=buf, reset=False)
+    buf2 = mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t)
+    for k, v in saved.items():
+        getattr(buf2, k).copy_(v)
+    _, g_rest = run_gpu(s, w_dev, mbs_dev, buf=buf2, reset=False)
+    for k in g_cont:
+        assert torch.equal(g_cont[k], g_rest[k]), k
+    # reset then one micro-batch equals the fresh result
+    _, g_reset = run_gpu(s, w_dev, mbs_dev, buf=buf)
+    for k in g1:
+        assert torch.equal(g_reset[k], g1[k]), k
+    # B = 0, b = 0: O = X + dropout(0) = X exactly
+    A, a, B, b = w_dev
+    outs0, _ = run_gpu(s, (A, a, torch.zeros_like(B), torch.zeros_like(b)), mbs_dev)
+    assert torch.equal(outs0[0]["O"], X.cpu())
+
+
+def test_bounded_wait_reports_timeout():
+    assert mlp.mlp_sync_status() == mlp.MLP_OK
+    mlp.mlp_wait_timeout_probe(1000000)   # 1 ms
+    assert mlp.mlp_sync_status() == mlp.MLP_ETIMEOUT
+    assert "bounded wait" in mlp.last_error()
+    assert mlp.mlp_sync_status() == mlp.MLP_OK  # the word is cleared, the context still works
+    x = torch.ones(16, device="cuda")
+    assert float(x.sum()) == 16.0
+
+
+def test_launch_counter_counts_kernels():
+    s = Shape(tokens=128, h=64, ffn=256, t=2, k=1)
+    w_dev, mbs_dev, _, _ = make_case(s)
+    buf = mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t)
+    n0 = mlp.mlp_launch_count()
+    mlp.block_step(s, w_dev, *mbs_dev[0], buf)
+    torch.cuda.synchronize()
+    # forward 2 GEMMs per slice; backward 1 + 5 per slice
+    assert mlp.mlp_launch_count() - n0 == 2 * s.t + 1 + 5 * s.t

@@ -1,0 +1,132 @@
+// HBM-bound kernels of the MLP block that do not fuse into a GEMM epilogue:
+//   * dropout backward + bias gradient:  dZ = dO * m / (1-p) (bf16),  db += sum_tok dZ
+//   * column sums:                        da_i += sum_tok dU_i
+//   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
+//
+// Column sums are deterministic: one CTA owns 64 columns for every row, each of
+// its 32 row-lanes sums a fixed row subset, and the 32 partial sums are added in
+// a fixed order.  Loads and stores are 16-byte vectors; a warp covers four
+// 128-byte row segments per instruction.
+#pragma once
+#include <cstdint>
+
+#include "block_math.cuh"
+#include "ptx.cuh"
+
+namespace gbmlp {
+
+constexpr int kColThreads = 256;  // 8 column groups (8 bf16 = 16 B each) x 32 row lanes
+constexpr int kColsPerCta = 64;
+
+// dZ = dO * keep * scale (rounded to bf16); db[c] += sum over rows of the rounded dZ.
+__global__ void __launch_bounds__(kColThreads)
+    k_dropout_bwd_colsum(const uint16_t* __restrict__ dO, uint16_t* __restrict__ dZ, float* __restrict__ db,
+                         int64_t rows, int cols, DropoutParams drop) {
+  __shared__ float part[32][kColsPerCta + 1];
+  const int cg = threadIdx.x & 7;
+  const int rl = threadIdx.x >> 3;
+  const int col = blockIdx.x * kColsPerCta + cg * 8;
+  float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (col < cols) {
+    for (int64_t r = rl; r < rows; r += 32) {
+      const int64_t off = r * cols + col;
+      const uint4 q = *reinterpret_cast<const uint4*>(dO + off);
+      float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
+                    bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool keep = dropout_keep(drop, r, col + j);
+        v[j] = round_bf16_f(keep ? v[j] * drop.scale : 0.0f);
+        s[j] += v[j];
+      }
+      uint4 o;
+      o.x = pack_bf16x2(v[0], v[1]);
+      o.y = pack_bf16x2(v[2], v[3]);
+      o.z = pack_bf16x2(v[4], v[5]);
+      o.w = pack_bf16x2(v[6], v[7]);
+      *reinterpret_cast<uint4*>(dZ + off) = o;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[rl][cg * 8 + j] = s[j];
+  __syncthreads();
+  if (threadIdx.x < kColsPerCta) {
+    const int c = blockIdx.x * kColsPerCta + threadIdx.x;
+    if (c < cols) {
+      float tot = 0.0f;
+      for (int k = 0; k < 32; ++k) tot += part[k][threadIdx.x];
+      db[c] += tot;
+    }
+  }
+}
+
+// out[c] += sum over rows of x[r * ld + c], c < cols.
+__global__ void __launch_bounds__(kColThreads)
+    k_colsum_bf16(const uint16_t* __restrict__ x, int64_t ld, float* __restrict__ out, int64_t rows, int cols) {
+  __shared__ float part[32][kColsPerCta + 1];
+  const int cg = threadIdx.x & 7;
+  const int rl = threadIdx.x >> 3;
+  const int col = blockIdx.x * kColsPerCta + cg * 8;
+  float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (col < cols) {
+    for (int64_t r = rl; r < rows; r += 32) {
+      const uint4 q = *reinterpret_cast<const uint4*>(x + r * ld + col);
+      s[0] += bf16lo(q.x); s[1] += bf16hi(q.x);
+      s[2] += bf16lo(q.y); s[3] += bf16hi(q.y);
+      s[4] += bf16lo(q.z); s[5] += bf16hi(q.z);
+      s[6] += bf16lo(q.w); s[7] += bf16hi(q.w);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[rl][cg * 8 + j] = s[j];
+  __syncthreads();
+  if (threadIdx.x < kColsPerCta) {
+    const int c = blockIdx.x * kColsPerCta + threadIdx.x;
+    if (c < cols) {
+      float tot = 0.0f;
+      for (int k = 0; k < 32; ++k) tot += part[k][threadIdx.x];
+      out[c] += tot;
+    }
+  }
+}
+
+// p[0 .. n) = 0 with 16-byte stores; n % 4 == 0 and p 16-byte aligned.
+__global__ void k_zero_f32(float* __restrict__ p, int64_t n) {
+  const int64_t n4 = n / 4;
+  float4* p4 = reinterpret_cast<float4*>(p);
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
+    p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// m[r * cols + c] = keep(r, c) ? 1 : 0.
+__global__ void k_dropout_mask(uint8_t* __restrict__ m, int64_t rows, int cols, DropoutParams drop) {
+  const int64_t n = rows * (int64_t)cols;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / cols;
+    const int64_t c = i - r * cols;
+    m[i] = dropout_keep(drop, r, c) ? 1 : 0;
+  }
+}
+
+// y = GeLU(x), dy = GeLU'(x) with the epilogues' device functions.
+__global__ void k_gelu_probe(const float* __restrict__ x, int64_t n, float* __restrict__ y, float* __restrict__ dy) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    y[i] = gelu_f(x[i]);
+    dy[i] = gelu_prime_f(x[i]);
+  }
+}
+
+// Waits on an mbarrier that nothing arrives on, with the given limit, and records
+// a timeout in the status word: exercises the bounded-wait error path.
+__global__ void k_wait_timeout_probe(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, limit_ns)) {
+      if (atomicCAS(status, 0, kStatusTimeout) == 0) status[1] = 99;
+    }
+  }
+}
+
+}  // namespace gbmlp

@@ -1,0 +1,501 @@
+// C-ABI of the tensor-sliced MLP block: argument checks, TMA descriptors and the
+// kernel sequence of the forward and backward passes on the caller's stream.
+//
+// Forward (per slice i, in turn):  F1  U_i, Y_i = GeLU(X A_i + a_i)        GEMM + GeLU epilogue
+//                                  F2  Z += Y_i B_i; last slice: O = R + dropout(Z + b)
+// Backward:                        B1  dZ = dropout'(dO), db += sum dZ       element-wise + column sum
+//                   (per slice)    B2  dU_i = (dZ B_i^T) * GeLU'(U_i)      GEMM + GeLU' epilogue
+//                                      da_i += sum dU_i                    column sum
+//                                  B3  dB_i += Y_i^T dZ                    GEMM + fp32 accumulate
+//                                  B4  dA_i += X^T dU_i                    GEMM + fp32 accumulate
+//                                  B5  dX (+)= dU_i A_i^T; last slice adds dO and writes bf16
+// The forward sum over slices (operator g of the Megatron MLP) and the backward sum
+// (operator f) are fp32 reductions in HBM on this GPU (STRONGHOLD slides, item 8).
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "elementwise.cuh"
+#include "gb_mlp.h"
+#include "gemm_tc.cuh"
+
+using namespace gbmlp;
+
+namespace {
+
+// Device status word: [0] = first error code, [1] = the site that recorded it.
+__device__ int g_status_word[2];
+
+thread_local std::string g_last_error;
+std::atomic<uint64_t> g_launches{0};
+
+// Optional per-launch timing: a CUDA event pair around every kernel launch.
+struct TraceEntry {
+  int kind;
+  int64_t m, n, k;
+};
+struct TraceState {
+  bool on = false;
+  int capacity = 0;
+  int count = 0;
+  cudaEvent_t* ev = nullptr;  // 2 * capacity events
+  TraceEntry* entries = nullptr;
+};
+std::mutex g_trace_mu;
+TraceState g_trace;
+
+// Kernel identifiers reported by the trace.
+enum TraceKind {
+  kTraceF1 = 0, kTraceF2 = 1, kTraceB2 = 2, kTraceB3 = 3, kTraceB4 = 4, kTraceB5 = 5,
+  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13
+};
+
+// Records the start event of the next launch; returns its slot or -1.
+int trace_pre(cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (!g_trace.on || g_trace.count >= g_trace.capacity) return -1;
+  const int slot = g_trace.count++;
+  cudaEventRecord(g_trace.ev[2 * slot], s);
+  return slot;
+}
+
+void trace_post(int slot, cudaStream_t s, int kind, int64_t m, int64_t n, int64_t k) {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  cudaEventRecord(g_trace.ev[2 * slot + 1], s);
+  g_trace.entries[slot] = TraceEntry{kind, m, n, k};
+}
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;
+  bool gemm_attr[3] = {false, false, false};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+// Current device, checked to be sm_103; sets up per-device state once.
+int device_state(DeviceState** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MLP_EUNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MLP_EUNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (major != 10 || minor != 3)
+      return fail(MLP_EUNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a only", dev, major, minor);
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status_word);
+    if (e != cudaSuccess) return fail(MLP_ECUDA, "status word address: %s", cudaGetErrorString(e));
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return fail(MLP_ECUDA, "cuTensorMapEncodeTiled unavailable");
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    st.sms = sms;
+    st.status = static_cast<int*>(p);
+    st.ready = true;
+  }
+  *out = &st;
+  return MLP_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows, row
+// pitch `ld` elements; box {box_inner, box_outer}; 128-byte swizzle; out-of-range
+// elements read as zero.
+int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
+             uint32_t box_outer) {
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled failed (%d): inner %lld outer %lld ld %lld", (int)r,
+                (long long)inner, (long long)outer, (long long)ld);
+  return MLP_OK;
+}
+
+// Tensor map of one GEMM operand with `mn` rows/columns along M (or N) and `k`
+// along the reduction.  K-major: k contiguous; MN-major: m (or n) contiguous.
+int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int64_t k, int64_t ld,
+                uint32_t tile_mn) {
+  if (mn_major) return make_map(m, base, mn, k, ld, 64, kBK);
+  return make_map(m, base, k, mn, ld, kBK, tile_mn);
+}
+
+template <bool AM, bool BM>
+int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtensorMap& mB, int M, int N, int K,
+                  const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+  auto kern = k_gemm_bf16_tc<AM, BM>;
+  if (!st->gemm_attr[slot]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+    if (e != cudaSuccess) return fail(MLP_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    st->gemm_attr[slot] = true;
+  }
+  const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
+  const int grid = (int)(tiles < st->sms ? tiles : st->sms);
+  const int ts = trace_pre(stream);
+  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(mA, mB, M, N, K, ep, st->status);
+  trace_post(ts, stream, trace_kind, M, N, K);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLP_ECUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  return MLP_OK;
+}
+
+// D[M, N] = A(M x K) B(K x N) with the given operand layouts and epilogue.
+int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, bool b_mn, int64_t ldb, int M, int N,
+         int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+  CUtensorMap mA, mB;
+  int rc = operand_map(&mA, a, a_mn, M, K, lda, kBM);
+  if (rc) return rc;
+  rc = operand_map(&mB, b, b_mn, N, K, ldb, kBN);
+  if (rc) return rc;
+  if (!a_mn && b_mn) return launch_gemm_t<false, true>(st, 0, mA, mB, M, N, K, ep, stream, trace_kind);
+  if (!a_mn && !b_mn) return launch_gemm_t<false, false>(st, 1, mA, mB, M, N, K, ep, stream, trace_kind);
+  if (a_mn && b_mn) return launch_gemm_t<true, true>(st, 2, mA, mB, M, N, K, ep, stream, trace_kind);
+  return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
+}
+
+DropoutParams make_dropout(float p, uint64_t seed, uint64_t token_offset, int h) {
+  DropoutParams d;
+  d.seed = seed;
+  d.token_offset = token_offset;
+  d.row_width = (uint64_t)h;
+  d.thr = (uint64_t)llround((double)p * 4294967296.0);
+  d.scale = 1.0f / (1.0f - p);
+  return d;
+}
+
+int check_shape(int h, int ffn, int t, int slice, int64_t tokens, float p) {
+  if (h <= 0 || h % 8 != 0) return fail(MLP_EINVAL, "h = %d must be positive and a multiple of 8", h);
+  if (t <= 0 || ffn <= 0 || ffn % t != 0) return fail(MLP_EINVAL, "ffn = %d must be a positive multiple of t = %d", ffn, t);
+  if ((ffn / t) % 8 != 0) return fail(MLP_EINVAL, "f = ffn / t = %d must be a multiple of 8", ffn / t);
+  if (tokens <= 0 || tokens >= (int64_t)1 << 31) return fail(MLP_EINVAL, "tokens = %lld out of range", (long long)tokens);
+  if (!(p >= 0.0f && p < 1.0f)) return fail(MLP_EINVAL, "dropout probability p = %g not in [0, 1)", (double)p);
+  if (slice < -1 || slice >= t) return fail(MLP_EINVAL, "slice = %d not in [-1, t = %d)", slice, t);
+  return MLP_OK;
+}
+
+int check_ptrs(const char* what, std::initializer_list<const void*> ptrs) {
+  int idx = 0;
+  for (const void* p : ptrs) {
+    if (p == nullptr) return fail(MLP_EINVAL, "%s: pointer argument %d is NULL", what, idx);
+    if (!aligned16(p)) return fail(MLP_EALIGN, "%s: pointer argument %d is not 16-byte aligned", what, idx);
+    ++idx;
+  }
+  return MLP_OK;
+}
+
+int launch_check(const char* what) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MLP_ECUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  return MLP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,
+            const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a, const mlp_bf16* B, const mlp_bf16* b,
+            const mlp_bf16* R, mlp_bf16* U, mlp_bf16* Y, float* Zacc, mlp_bf16* O, void* stream) {
+  int rc = check_shape(h, ffn, t, slice, tokens, p);
+  if (rc) return rc;
+  rc = check_ptrs("mlp_fwd", {X, A, a, B, b, U, Y, O});
+  if (rc) return rc;
+  if (R != nullptr && !aligned16(R)) return fail(MLP_EALIGN, "mlp_fwd: R is not 16-byte aligned");
+  if (t > 1) {
+    rc = check_ptrs("mlp_fwd (Zacc, needed when t > 1)", {Zacc});
+    if (rc) return rc;
+  }
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int f = ffn / t;
+  const int T = (int)tokens;
+  const DropoutParams drop = make_dropout(p, seed, token_offset, h);
+  if (R == nullptr) R = X;
+  const int i0 = slice < 0 ? 0 : slice;
+  const int i1 = slice < 0 ? t : slice + 1;
+  for (int i = i0; i < i1; ++i) {
+    // F1: U_i = X A_i + a_i, Y_i = GeLU(U_i)          (M = T, N = f, K = h)
+    EpiParams e1{};
+    e1.kind = kEpiGelu;
+    e1.ld = ffn;
+    e1.out0 = U + (int64_t)i * f;
+    e1.out1 = Y + (int64_t)i * f;
+    e1.bias = a + (int64_t)i * f;
+    rc = gemm(st, X, false, h, A + (int64_t)i * f, true, ffn, T, f, h, e1, s, kTraceF1);
+    if (rc) return rc;
+    // F2: Z (+)= Y_i B_i; the last slice finishes O = R + dropout(Z + b)   (M = T, N = h, K = f)
+    EpiParams e2{};
+    e2.ld = h;
+    if (t == 1 || i == t - 1) {
+      e2.kind = kEpiDropRes;
+      e2.g_in = (t == 1) ? nullptr : Zacc;
+      e2.in0 = R;
+      e2.bias = b;
+      e2.out0 = O;
+      e2.drop = drop;
+    } else {
+      e2.kind = (i == 0) ? kEpiF32Store : kEpiF32Add;
+      e2.g_out = Zacc;
+    }
+    rc = gemm(st, Y + (int64_t)i * f, false, ffn, B + (int64_t)i * f * h, true, h, T, h, f, e2, s, kTraceF2);
+    if (rc) return rc;
+  }
+  return MLP_OK;
+}
+
+int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,
+            int residual_grad, const mlp_bf16* dO, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
+            const mlp_bf16* U, const mlp_bf16* Y, mlp_bf16* dZ, mlp_bf16* dU, float* dXacc, mlp_bf16* dX,
+            float* dA, float* da, float* dB, float* db, void* stream) {
+  int rc = check_shape(h, ffn, t, slice, tokens, p);
+  if (rc) return rc;
+  rc = check_ptrs("mlp_bwd", {dO, X, A, B, U, Y, dZ, dU, dX, dA, da, dB, db});
+  if (rc) return rc;
+  if (t > 1) {
+    rc = check_ptrs("mlp_bwd (dXacc, needed when t > 1)", {dXacc});
+    if (rc) return rc;
+  }
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int f = ffn / t;
+  const int T = (int)tokens;
+  const DropoutParams drop = make_dropout(p, seed, token_offset, h);
+  if (slice <= 0) {
+    // B1: dZ = dO * m / (1 - p), db += sum_tok dZ
+    const int ts = trace_pre(s);
+    k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dO, dZ, db, tokens, h, drop);
+    trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
+    rc = launch_check("dropout backward");
+    if (rc) return rc;
+  }
+  const int i0 = slice < 0 ? 0 : slice;
+  const int i1 = slice < 0 ? t : slice + 1;
+  for (int i = i0; i < i1; ++i) {
+    const int64_t c = (int64_t)i * f;
+    // B2: dU_i = (dZ B_i^T) * GeLU'(U_i)                 (M = T, N = f, K = h)
+    EpiParams e2{};
+    e2.kind = kEpiDGelu;
+    e2.ld = ffn;
+    e2.in0 = U + c;
+    e2.out0 = dU + c;
+    rc = gemm(st, dZ, false, h, B + c * h, false, h, T, f, h, e2, s, kTraceB2);
+    if (rc) return rc;
+    // da_i += sum_tok dU_i
+    const int ts = trace_pre(s);
+    k_colsum_bf16<<<(f + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dU + c, ffn, da + c, tokens, f);
+    trace_post(ts, s, kTraceColsum, tokens, f, 0);
+    rc = launch_check("bias-gradient column sum");
+    if (rc) return rc;
+    // B3: dB_i += Y_i^T dZ                               (M = f, N = h, K = T)
+    EpiParams e3{};
+    e3.kind = kEpiF32Add;
+    e3.ld = h;
+    e3.g_out = dB + c * h;
+    rc = gemm(st, Y + c, true, ffn, dZ, true, h, f, h, T, e3, s, kTraceB3);
+    if (rc) return rc;
+    // B4: dA_i += X^T dU_i                               (M = h, N = f, K = T)
+    EpiParams e4{};
+    e4.kind = kEpiF32Add;
+    e4.ld = ffn;
+    e4.g_out = dA + c;
+    rc = gemm(st, X, true, h, dU + c, true, ffn, h, f, T, e4, s, kTraceB4);
+    if (rc) return rc;
+    // B5: dX (+)= dU_i A_i^T; the last slice adds dO and writes bf16   (M = T, N = h, K = f)
+    EpiParams e5{};
+    e5.ld = h;
+    if (t == 1 || i == t - 1) {
+      e5.kind = kEpiResAdd;
+      e5.g_in = (t == 1) ? nullptr : dXacc;
+      e5.in0 = residual_grad ? dO : nullptr;
+      e5.out0 = dX;
+    } else {
+      e5.kind = (i == 0) ? kEpiF32Store : kEpiF32Add;
+      e5.g_out = dXacc;
+    }
+    rc = gemm(st, dU + c, false, ffn, A + c, false, ffn, T, h, f, e5, s, kTraceB5);
+    if (rc) return rc;
+  }
+  return MLP_OK;
+}
+
+int grad_accum_reset(int h, int ffn, float* dA, float* da, float* dB, float* db, void* stream) {
+  if (h <= 0 || h % 8 != 0 || ffn <= 0 || ffn % 8 != 0)
+    return fail(MLP_EINVAL, "grad_accum_reset: h = %d and ffn = %d must be positive multiples of 8", h, ffn);
+  int rc = check_ptrs("grad_accum_reset", {dA, da, dB, db});
+  if (rc) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* bufs[4] = {dA, da, dB, db};
+  const int64_t sizes[4] = {(int64_t)h * ffn, ffn, (int64_t)ffn * h, h};
+  for (int k = 0; k < 4; ++k) {
+    const int64_t n4 = sizes[k] / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    if (blocks > (int64_t)st->sms * 8) blocks = (int64_t)st->sms * 8;
+    if (blocks < 1) blocks = 1;
+    const int ts = trace_pre(s);
+    k_zero_f32<<<(int)blocks, 256, 0, s>>>(bufs[k], sizes[k]);
+    trace_post(ts, s, kTraceZero, sizes[k], 0, 0);
+    rc = launch_check("grad_accum_reset");
+    if (rc) return rc;
+  }
+  return MLP_OK;
+}
+
+int mlp_sync_status(void* stream) {
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(MLP_ECUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  int word[2] = {0, 0};
+  e = cudaMemcpy(word, st->status, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(MLP_ECUDA, "status read: %s", cudaGetErrorString(e));
+  if (word[0] != 0) {
+    const int zero[2] = {0, 0};
+    cudaMemcpy(st->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    return fail(word[0], "a kernel gave up on a bounded wait (site %d)", word[1]);
+  }
+  return MLP_OK;
+}
+
+const char* mlp_last_error(void) { return g_last_error.c_str(); }
+
+int mlp_dropout_mask(int h, int64_t tokens, float p, uint64_t seed, uint64_t token_offset, uint8_t* m,
+                     void* stream) {
+  if (h <= 0 || tokens <= 0 || tokens >= (int64_t)1 << 31 || !(p >= 0.0f && p < 1.0f))
+    return fail(MLP_EINVAL, "mlp_dropout_mask: bad h, tokens or p");
+  if (m == nullptr) return fail(MLP_EINVAL, "mlp_dropout_mask: m is NULL");
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  const DropoutParams drop = make_dropout(p, seed, token_offset, h);
+  k_dropout_mask<<<st->sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(m, tokens, h, drop);
+  return launch_check("dropout mask");
+}
+
+int mlp_gelu_probe(const float* x, int64_t n, float* y, float* dy, void* stream) {
+  if (n <= 0 || x == nullptr || y == nullptr || dy == nullptr) return fail(MLP_EINVAL, "mlp_gelu_probe: bad arguments");
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  k_gelu_probe<<<st->sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, n, y, dy);
+  return launch_check("gelu probe");
+}
+
+int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream) {
+  if (limit_ns > 1000000000ull) return fail(MLP_EINVAL, "mlp_wait_timeout_probe: limit above one second");
+  DeviceState* st = nullptr;
+  int rc = device_state(&st);
+  if (rc) return rc;
+  k_wait_timeout_probe<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status, limit_ns);
+  return launch_check("wait-timeout probe");
+}
+
+uint64_t mlp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mlp_trace_begin(int capacity) {
+  if (capacity <= 0 || capacity > (1 << 20)) return fail(MLP_EINVAL, "mlp_trace_begin: capacity %d out of range", capacity);
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (g_trace.on) return fail(MLP_EINVAL, "mlp_trace_begin: a trace is already running");
+  g_trace.ev = new cudaEvent_t[2 * (size_t)capacity];
+  g_trace.entries = new TraceEntry[capacity];
+  for (int i = 0; i < 2 * capacity; ++i) {
+    cudaError_t e = cudaEventCreate(&g_trace.ev[i]);
+    if (e != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(g_trace.ev[j]);
+      delete[] g_trace.ev;
+      delete[] g_trace.entries;
+      g_trace.ev = nullptr;
+      g_trace.entries = nullptr;
+      return fail(MLP_ECUDA, "mlp_trace_begin: cudaEventCreate: %s", cudaGetErrorString(e));
+    }
+  }
+  g_trace.capacity = capacity;
+  g_trace.count = 0;
+  g_trace.on = true;
+  return MLP_OK;
+}
+
+int mlp_trace_end(int max_entries, int* kinds, int64_t* mnk, float* ms) {
+  std::lock_guard<std::mutex> lock(g_trace_mu);
+  if (!g_trace.on) return fail(MLP_EINVAL, "mlp_trace_end: no trace is running");
+  g_trace.on = false;
+  const int n = g_trace.count < max_entries ? g_trace.count : max_entries;
+  int rc = n;
+  for (int i = 0; i < n; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_trace.ev[2 * i + 1]);
+    float t = 0.0f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, g_trace.ev[2 * i], g_trace.ev[2 * i + 1]);
+    if (e != cudaSuccess) {
+      rc = fail(MLP_ECUDA, "mlp_trace_end: %s", cudaGetErrorString(e));
+      break;
+    }
+    if (kinds) kinds[i] = g_trace.entries[i].kind;
+    if (mnk) {
+      mnk[3 * i] = g_trace.entries[i].m;
+      mnk[3 * i + 1] = g_trace.entries[i].n;
+      mnk[3 * i + 2] = g_trace.entries[i].k;
+    }
+    if (ms) ms[i] = t;
+  }
+  for (int i = 0; i < 2 * g_trace.capacity; ++i) cudaEventDestroy(g_trace.ev[i]);
+  delete[] g_trace.ev;
+  delete[] g_trace.entries;
+  g_trace.ev = nullptr;
+  g_trace.entries = nullptr;
+  g_trace.capacity = 0;
+  g_trace.count = 0;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,364 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
+//
+//   D[M, N] = sum_k A(m, k) * B(n, k)       (bf16 operands, fp32 accumulator in TMEM)
+//
+// Operands live row-major in HBM; each may be K-major (k contiguous) or MN-major
+// (m or n contiguous), so the six contractions of the MLP block's forward and
+// backward never materialise a transpose.  Tiles are BM x BN = 128 x 256 with
+// BK = 64 (one 128-byte swizzle atom of bf16 along the contiguous dimension).
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: loads A/B k-blocks into a STAGES-deep smem ring.
+//   warp 1      TMEM owner and MMA issuer: one thread issues tcgen05.mma; the
+//               accumulator is double-buffered (2 x BN fp32 columns of TMEM) so
+//               the epilogue of tile j overlaps the main loop of tile j+1.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lane
+//               quarter w % 4, i.e. tile rows 32*(w%4) .. +31), fused element-wise
+//               work, vectorised global stores.
+// Every mbarrier wait is bounded; on timeout the kernel records kStatusTimeout in
+// the status word, drains its own copies and MMAs, frees TMEM and returns.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "block_math.cuh"
+#include "ptx.cuh"
+
+namespace gbmlp {
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KB
+constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KB
+constexpr uint32_t kChunkBytes = 64 * kBK * 2;       // one 64 x BK box of an MN-major operand
+constexpr uint32_t kTmemCols = 2 * kBN;              // double-buffered accumulator
+constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+enum EpiKind : int {
+  kEpiGelu = 0,      // U = acc + bias (bf16), Y = GeLU(acc + bias) (bf16)
+  kEpiF32Store = 1,  // G = acc (fp32)
+  kEpiF32Add = 2,    // G += acc (fp32 read-modify-write)
+  kEpiDropRes = 3,   // O = R + dropout((G ? G : 0) + acc + bias) (bf16)
+  kEpiDGelu = 4,     // dU = acc * GeLU'(U) (bf16)
+  kEpiResAdd = 5,    // dX = (G ? G : 0) + acc + (R ? R : 0) (bf16)
+};
+
+struct EpiParams {
+  int kind;
+  int64_t ld;                 // leading dimension (elements) shared by every tensor the epilogue touches
+  float* g_out;               // fp32 output (F32Store / F32Add)
+  const float* g_in;          // fp32 partial sum read by DropRes / ResAdd (may be null)
+  uint16_t* out0;             // bf16 output: U / O / dU / dX
+  uint16_t* out1;             // bf16 output: Y
+  const uint16_t* in0;        // bf16 input: R (DropRes, ResAdd) or U (DGelu); may be null for ResAdd
+  const uint16_t* bias;       // bias vector indexed by output column
+  DropoutParams drop;
+};
+
+__device__ __forceinline__ void st_bf16x8(uint16_t* p, const float (&v)[8]) {
+  uint4 q;
+  q.x = pack_bf16x2(v[0], v[1]);
+  q.y = pack_bf16x2(v[2], v[3]);
+  q.z = pack_bf16x2(v[4], v[5]);
+  q.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = q;
+}
+
+__device__ __forceinline__ void ld_bf16x8(const uint16_t* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf16lo(q.x); v[1] = bf16hi(q.x);
+  v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+  v[4] = bf16lo(q.z); v[5] = bf16hi(q.z);
+  v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+}
+
+__device__ __forceinline__ void ld_f32x8(const float* p, float (&v)[8]) {
+  const float4 a = reinterpret_cast<const float4*>(p)[0];
+  const float4 b = reinterpret_cast<const float4*>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void st_f32x8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// One thread, one row, 32 accumulator columns [col0, col0 + 32).  N % 8 == 0.
+template <int KIND>
+__device__ __forceinline__ void epilogue_chunk(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
+                                               int N) {
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    const int col = col0 + 8 * g;
+    if (col >= N) break;
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[8 * g + j]);
+    const int64_t off = row * ep.ld + col;
+    if constexpr (KIND == kEpiGelu) {
+      float bb[8], y[8];
+      ld_bf16x8(ep.bias + col, bb);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[j] += bb[j];
+        y[j] = gelu_f(v[j]);
+      }
+      st_bf16x8(ep.out0 + off, v);
+      st_bf16x8(ep.out1 + off, y);
+    } else if constexpr (KIND == kEpiF32Store) {
+      st_f32x8(ep.g_out + off, v);
+    } else if constexpr (KIND == kEpiF32Add) {
+      float o[8];
+      ld_f32x8(ep.g_out + off, o);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o[j] += v[j];
+      st_f32x8(ep.g_out + off, o);
+    } else if constexpr (KIND == kEpiDropRes) {
+      float bb[8], res[8];
+      if (ep.g_in != nullptr) {
+        float z[8];
+        ld_f32x8(ep.g_in + off, z);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = z[j] + v[j];
+      }
+      ld_bf16x8(ep.bias + col, bb);
+      ld_bf16x8(ep.in0 + off, res);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool keep = dropout_keep(ep.drop, row, col + j);
+        v[j] = res[j] + (keep ? (v[j] + bb[j]) * ep.drop.scale : 0.0f);
+      }
+      st_bf16x8(ep.out0 + off, v);
+    } else if constexpr (KIND == kEpiDGelu) {
+      float u[8];
+      ld_bf16x8(ep.in0 + off, u);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] *= gelu_prime_f(u[j]);
+      st_bf16x8(ep.out0 + off, v);
+    } else if constexpr (KIND == kEpiResAdd) {
+      if (ep.g_in != nullptr) {
+        float z[8];
+        ld_f32x8(ep.g_in + off, z);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = z[j] + v[j];
+      }
+      if (ep.in0 != nullptr) {
+        float res[8];
+        ld_bf16x8(ep.in0 + off, res);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] += res[j];
+      }
+      st_bf16x8(ep.out0 + off, v);
+    }
+  }
+}
+
+__device__ __forceinline__ void epilogue_dispatch(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
+                                                  int N) {
+  switch (ep.kind) {
+    case kEpiGelu: epilogue_chunk<kEpiGelu>(ep, row, col0, r, N); break;
+    case kEpiF32Store: epilogue_chunk<kEpiF32Store>(ep, row, col0, r, N); break;
+    case kEpiF32Add: epilogue_chunk<kEpiF32Add>(ep, row, col0, r, N); break;
+    case kEpiDropRes: epilogue_chunk<kEpiDropRes>(ep, row, col0, r, N); break;
+    case kEpiDGelu: epilogue_chunk<kEpiDGelu>(ep, row, col0, r, N); break;
+    default: epilogue_chunk<kEpiResAdd>(ep, row, col0, r, N); break;
+  }
+}
+
+__device__ __forceinline__ void record_status(int* status, int code, int site) {
+  if (status != nullptr) {
+    if (atomicCAS(status, 0, code) == 0) status[1] = site;
+  }
+}
+
+// A_MN / B_MN: operand stored MN-major (true) or K-major (false).
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
+                   int K, EpiParams ep, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_full = empty + kStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* mma_done = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_m = (M + kBM - 1) / kBM;
+  const int num_n = (N + kBN - 1) / kBN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (K + kBK - 1) / kBK;
+
+  // A pipeline that broke in an earlier launch leaves the status word set; later
+  // launches then skip their work so that a failure ends quickly.
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) {
+    s_skip = (status != nullptr && *reinterpret_cast<volatile int*>(status) != 0) ? 1 : 0;
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int tile_end = s_skip ? 0 : num_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t issued[kStages];
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tile_end && ok; tile += gridDim.x) {
+        const int m0 = (tile % num_m) * kBM;
+        const int n0 = (tile / num_m) * kBN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1)) {
+            record_status(status, kStatusTimeout, 1);
+            ok = false;
+            break;
+          }
+          const int k0 = kb * kBK;
+          mbar_arrive_expect_tx(&full[stage], kStageBytes);
+          uint8_t* a_dst = sA + stage * kABytes;
+          uint8_t* b_dst = sB + stage * kBBytes;
+          if constexpr (A_MN) {
+#pragma unroll
+            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(a_dst + j * kChunkBytes, &tmA, &full[stage], m0 + 64 * j, k0);
+          } else {
+            tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+          }
+          if constexpr (B_MN) {
+#pragma unroll
+            for (int j = 0; j < kBN / 64; ++j) tma_load_2d(b_dst + j * kChunkBytes, &tmB, &full[stage], n0 + 64 * j, k0);
+          } else {
+            tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
+          }
+          ++issued[stage];
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // Drain: every copy this thread issued has landed before the CTA may exit.
+      for (int s = 0; s < kStages; ++s) {
+        if (issued[s] > 0 && !mbar_wait(&full[s], (issued[s] - 1) & 1)) record_status(status, kStatusTimeout, 2);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tile_end && ok; tile += gridDim.x) {
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
+          record_status(status, kStatusTimeout, 3);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase)) {
+            record_status(status, kStatusTimeout, 4);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * kABytes);
+          const uint32_t b_base = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t adesc = A_MN ? make_sdesc_sw128(a_base + kk * 2048, kChunkBytes, 1024)
+                                        : make_sdesc_sw128(a_base + kk * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? make_sdesc_sw128(b_base + kk * 2048, kChunkBytes, 1024)
+                                        : make_sdesc_sw128(b_base + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[stage]);  // the smem stage is free once these MMAs have read it
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&acc_full[acc]);  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      umma_commit(mma_done);
+      if (!mbar_wait(mma_done, 0)) record_status(status, kStatusTimeout, 5);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int row_in_tile = quarter * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < tile_end; tile += gridDim.x) {
+      const int m0 = (tile % num_m) * kBM;
+      const int n0 = (tile / num_m) * kBN;
+      if (!mbar_wait(&acc_full[acc], acc_phase)) {
+        record_status(status, kStatusTimeout, 6);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = (int64_t)m0 + row_in_tile;
+      const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c0, r);
+        tmem_ld_wait();
+        if (row < M && n0 + c0 < N) epilogue_dispatch(ep, row, n0 + c0, r, N);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace gbmlp
