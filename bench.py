@@ -306,8 +306,8 @@ def run_ours(args, wl, rank, world, dist):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="mtnlg")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--slice-mode", default="all", choices=["all", "each"])

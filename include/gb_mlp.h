@@ -66,18 +66,22 @@ enum {
 /*
  * mlp_fwd - forward of one micro-batch (STRONGHOLD slides, items 7-8).
  *
- *   slice == -1: all t slices in turn inside this call.
+ *   slice == -1: all t slices inside this call.  Each GEMM launch covers every
+ *                slice: the first walks the column blocks A_0 .. A_{t-1}, the
+ *                second's reduction loop walks the row blocks B_0 .. B_{t-1}, so
+ *                the sum over slices is formed in the fp32 accumulator on chip.
+ *                Zacc is not used (may be NULL).
  *   slice == i : slice i only.  Calls must come in order i = 0 .. t-1 on one
  *                stream; slice 0 overwrites Zacc, slices 0 .. t-2 accumulate
- *                into it, and slice t-1 writes O.
+ *                into it (fp32, in HBM), and slice t-1 writes O.
  *   X      [tokens, h]   input activations.
  *   A, a   [h, ffn], [ffn]   first weight and bias (slice i = columns i*f ..).
  *   B, b   [ffn, h], [h]     second weight and bias (slice i = rows i*f ..).
  *   R      [tokens, h]   residual; NULL means R = X.
  *   U, Y   [tokens, ffn] outputs: pre-activation and GeLU output (bf16), kept
  *                        for the backward; slice i writes columns i*f .. .
- *   Zacc   [tokens, h] fp32 workspace for the sum over slices; may be NULL
- *                        when t == 1.
+ *   Zacc   [tokens, h] fp32 workspace for the sum over slices of one-slice
+ *                        calls; may be NULL when t == 1 or slice == -1.
  *   O      [tokens, h]   output, written by the last slice.
  * Returns MLP_OK or an error code.
  */
@@ -90,15 +94,17 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
  * (+=) into the fp32 dA, da, dB, db (gradient accumulation over micro-batches).
  *
  *   slice == -1 or slice == i as for mlp_fwd (order 0 .. t-1).  The call with
- *   slice 0 (or -1) computes dZ and db; the call with slice t-1 writes dX.
+ *   slice 0 (or -1) computes dZ and db; the call with slice t-1 (or -1) writes
+ *   dX.  With slice == -1 the sum over slices of dU_i A_i^T is formed in the
+ *   fp32 accumulator on chip and dXacc is not used.
  *   residual_grad  1: dX = dO + sum_i dU_i A_i^T (the residual R was X);
  *                  0: dX = sum_i dU_i A_i^T.
  *   dO     [tokens, h]  upstream gradient of O.
  *   X, A, B           as passed to mlp_fwd; U, Y as written by mlp_fwd.
  *   dZ     [tokens, h]  workspace/output: gradient after dropout (bf16).
  *   dU     [tokens, ffn] workspace/output: gradient of the pre-activation (bf16).
- *   dXacc  [tokens, h] fp32 workspace for the sum over slices; may be NULL when
- *                        t == 1.
+ *   dXacc  [tokens, h] fp32 workspace for the sum over slices of one-slice
+ *                        calls; may be NULL when t == 1 or slice == -1.
  *   dX     [tokens, h]  output (overwritten).
  *   dA, da, dB, db    fp32 gradient accumulators (+=).
  * Returns MLP_OK or an error code.

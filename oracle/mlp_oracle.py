@@ -195,26 +195,57 @@ def mlp_bwd(dO, X, A, B, U, Y, keep, t, p, mirror=False, residual_is_input=True)
 
 # ----------------------------------------------------------------------------
 # Sampled evaluation for workloads too large for the full oracle.  Each output
-# is computed from its definition alone (a token row, or a weight-gradient
-# column over all tokens); no slicing is needed since the sum over slices of
-# row-split partial products is the full product.
+# is computed from its definition alone: a token row of O / dX (the row loops over
+# the slices exactly as the block does), or a weight-gradient entry as a sum over
+# all tokens of one column of Y or dU.
 # ----------------------------------------------------------------------------
-def rows_fwd_bwd(rows, X, dO, A, a, B, b, p, seed, token_offset=0, mirror=False):
-    """O, dX, U, Y, dU rows for the given token rows (residual R = X)."""
+class Bf16Matrix:
+    """A bf16 matrix kept as raw bits; indexing returns the exact float64 values of
+    the selected block only (so a 3 GB weight never needs a 13 GB float64 copy)."""
+
+    def __init__(self, bits):
+        self.bits = np.asarray(bits, dtype=np.uint16)
+        self.shape = self.bits.shape
+
+    def __getitem__(self, idx):
+        return bf16_to_f64(self.bits[idx])
+
+
+def rows_fwd_bwd(rows, X, dO, A, a, B, b, t, p, seed, token_offset=0, mirror=False):
+    """O, dX, U, Y, dU, dZ rows for the given token rows (residual R = X).
+
+    X, dO, A, B may be float64 arrays or ``Bf16Matrix``; only slice-sized blocks
+    of A and B are decoded at a time."""
     rows = np.asarray(rows)
     h = X.shape[1]
+    F = A.shape[1]
+    f = F // t
     Xr = X[rows]
-    Ur = Xr @ A + a
-    Yr = _rb(gelu(Ur), mirror)
-    Urs = _rb(Ur, mirror)
-    Zr = Yr @ B
+    dOr = dO[rows]
     keep = dropout_keep(X.shape[0], h, p, seed, token_offset, rows=rows)
     s = dropout_scale(p)
+    dZr = _rb(np.where(keep, dOr * s, 0.0), mirror)
+    Zr = np.zeros((len(rows), h))
+    dXs = np.zeros((len(rows), h))
+    Ur_all = np.empty((len(rows), F))
+    Yr_all = np.empty((len(rows), F))
+    dUr_all = np.empty((len(rows), F))
+    for i in range(t):
+        cols = slice(i * f, (i + 1) * f)
+        A_i = A[:, cols]
+        B_i = B[cols, :]
+        Ur = Xr @ A_i + a[cols]
+        Yr = _rb(gelu(Ur), mirror)
+        Urs = _rb(Ur, mirror)
+        Zr += Yr @ B_i
+        dUr = _rb((dZr @ B_i.T) * gelu_prime(Urs), mirror)
+        dXs += dUr @ A_i.T
+        Ur_all[:, cols] = Urs
+        Yr_all[:, cols] = Yr
+        dUr_all[:, cols] = dUr
     Or = _rb(Xr + np.where(keep, (Zr + b) * s, 0.0), mirror)
-    dZr = _rb(np.where(keep, dO[rows] * s, 0.0), mirror)
-    dUr = _rb((dZr @ B.T) * gelu_prime(Urs), mirror)
-    dXr = _rb(dO[rows] + dUr @ A.T, mirror)
-    return {"O": Or, "dX": dXr, "U": Urs, "Y": Yr, "dU": dUr, "dZ": dZr, "keep": keep}
+    dXr = _rb(dOr + dXs, mirror)
+    return {"O": Or, "dX": dXr, "U": Ur_all, "Y": Yr_all, "dU": dUr_all, "dZ": dZr, "keep": keep}
 
 
 def full_dZ(dO, p, seed, token_offset=0, mirror=False):
@@ -225,6 +256,7 @@ def full_dZ(dO, p, seed, token_offset=0, mirror=False):
 
 def columns_U(cols, X, A, a, mirror=False):
     """U[:, cols] over all tokens (as stored) and the unrounded pre-activation."""
+    cols = np.asarray(cols)
     Uc = X @ A[:, cols] + a[cols]
     return _rb(Uc, mirror), Uc
 
@@ -242,6 +274,7 @@ def wgrad_dB_entries(r_idx, c_idx, X, A, a, dZ, mirror=False):
 
 def columns_dU(cols, X, A, a, B, dZ, mirror=False):
     """dU[:, cols] over all tokens."""
+    cols = np.asarray(cols)
     Us, _ = columns_U(cols, X, A, a, mirror)
     return _rb((dZ @ B[cols, :].T) * gelu_prime(Us), mirror)
 

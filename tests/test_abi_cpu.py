@@ -66,7 +66,7 @@ def _fwd(lib, h=64, ffn=256, t=2, slice_=-1, tokens=16, p=0.1, ptr=GOOD, R=None,
     (dict(ptr=None), mlp.MLP_EINVAL),
     (dict(ptr=GOOD + 2), mlp.MLP_EALIGN),
     (dict(R=GOOD + 8), mlp.MLP_EALIGN),
-    (dict(Zacc=None), mlp.MLP_EINVAL),             # t > 1 needs the fp32 workspace
+    (dict(Zacc=None, slice_=0), mlp.MLP_EINVAL),   # one-slice calls with t > 1 need the fp32 workspace
 ])
 def test_fwd_rejects_bad_arguments(lib, kw, code):
     assert _fwd(lib, **kw) == code
@@ -80,7 +80,8 @@ def test_bwd_rejects_bad_arguments(lib):
     bad[0] = 20
     assert lib.mlp_bwd(*bad) == mlp.MLP_EINVAL
     bad = list(args)
-    bad[17] = None                                   # dXacc is needed when t > 1
+    bad[3] = 0                                       # one-slice call with t > 1 ...
+    bad[17] = None                                   # ... needs the dXacc workspace
     assert lib.mlp_bwd(*bad) == mlp.MLP_EINVAL
     bad = list(args)
     bad[9] = g + 4                                   # dO misaligned
@@ -99,6 +100,7 @@ def test_valid_call_without_gpu_reports_unsupported(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert _fwd(lib) == mlp.MLP_EUNSUPPORTED
+    assert _fwd(lib, Zacc=None) == mlp.MLP_EUNSUPPORTED   # all-slices calls need no workspace
     assert mlp.mlp_launch_count() == 0
 
 

@@ -265,10 +265,19 @@ def test_sampled_evaluators_match_full_oracle():
         fw = orc.mlp_fwd(X, A, a, B, b, t, p, 1234, token_offset=off, mirror=mirror)
         bw = orc.mlp_bwd(dO, X, A, B, fw["U"], fw["Y"], fw["keep"], t, p, mirror=mirror)
         rows = [0, 5, 39]
-        r = orc.rows_fwd_bwd(rows, X, dO, A, a, B, b, p, 1234, token_offset=off, mirror=mirror)
-        np.testing.assert_allclose(r["O"], fw["O"][rows], rtol=1e-12, atol=1e-12)
-        np.testing.assert_allclose(r["dX"], bw["dX"][rows], rtol=1e-12, atol=1e-12)
-        np.testing.assert_allclose(r["dU"], bw["dU"][rows], rtol=1e-12, atol=1e-12)
+        for tt in (1, t):
+            r = orc.rows_fwd_bwd(rows, X, dO, A, a, B, b, tt, p, 1234, token_offset=off, mirror=mirror)
+            np.testing.assert_allclose(r["O"], fw["O"][rows], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(r["dX"], bw["dX"][rows], rtol=1e-12, atol=1e-12)
+            for key in ("dU", "U", "Y"):
+                src = bw if key == "dU" else fw
+                np.testing.assert_allclose(r[key], src[key][rows], rtol=1e-12, atol=1e-12)
+        # the lazily decoded bf16 form gives identical values
+        Ab = orc.Bf16Matrix(orc.f64_to_bf16_bits(A))
+        Bb = orc.Bf16Matrix(orc.f64_to_bf16_bits(B))
+        r2 = orc.rows_fwd_bwd(rows, X, dO, Ab, a, Bb, b, t, p, 1234, token_offset=off, mirror=mirror)
+        np.testing.assert_array_equal(r2["O"], r["O"])
+        np.testing.assert_array_equal(r2["dX"], r["dX"])
         dZ = orc.full_dZ(dO, p, 1234, token_offset=off, mirror=mirror)
         np.testing.assert_array_equal(dZ, bw["dZ"])
         ri = np.array([0, 95, 50, 7])

@@ -154,6 +154,22 @@ int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int
   return MLP_OK;
 }
 
+// 2-D fp32 tensor map of a GEMM output for TMA stores / reduce-adds: box of 32
+// columns x 32 rows, 128-byte swizzle.
+int make_out_map(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, int64_t ld) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled (fp32 output) failed (%d): cols %lld rows %lld ld %lld", (int)r,
+                (long long)cols, (long long)rows, (long long)ld);
+  return MLP_OK;
+}
+
 // Tensor map of one GEMM operand with `mn` rows/columns along M (or N) and `k`
 // along the reduction.  K-major: k contiguous; MN-major: m (or n) contiguous.
 int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int64_t k, int64_t ld,
@@ -163,8 +179,8 @@ int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int
 }
 
 template <bool AM, bool BM>
-int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtensorMap& mB, int M, int N, int K,
-                  const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
+                  int M, int N, int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
   auto kern = k_gemm_bf16_tc<AM, BM>;
   if (!st->gemm_attr[slot]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
@@ -174,7 +190,7 @@ int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtens
   const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
   const int grid = (int)(tiles < st->sms ? tiles : st->sms);
   const int ts = trace_pre(stream);
-  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(mA, mB, M, N, K, ep, st->status);
+  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(mA, mB, mC, M, N, K, ep, st->status);
   trace_post(ts, stream, trace_kind, M, N, K);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   cudaError_t e = cudaGetLastError();
@@ -185,14 +201,20 @@ int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtens
 // D[M, N] = A(M x K) B(K x N) with the given operand layouts and epilogue.
 int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, bool b_mn, int64_t ldb, int M, int N,
          int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mC;
   int rc = operand_map(&mA, a, a_mn, M, K, lda, kBM);
   if (rc) return rc;
   rc = operand_map(&mB, b, b_mn, N, K, ldb, kBN);
   if (rc) return rc;
-  if (!a_mn && b_mn) return launch_gemm_t<false, true>(st, 0, mA, mB, M, N, K, ep, stream, trace_kind);
-  if (!a_mn && !b_mn) return launch_gemm_t<false, false>(st, 1, mA, mB, M, N, K, ep, stream, trace_kind);
-  if (a_mn && b_mn) return launch_gemm_t<true, true>(st, 2, mA, mB, M, N, K, ep, stream, trace_kind);
+  if (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add) {
+    rc = make_out_map(&mC, ep.g_out, N, M, ep.ld);
+    if (rc) return rc;
+  } else {
+    memset(&mC, 0, sizeof(mC));
+  }
+  if (!a_mn && b_mn) return launch_gemm_t<false, true>(st, 0, mA, mB, mC, M, N, K, ep, stream, trace_kind);
+  if (!a_mn && !b_mn) return launch_gemm_t<false, false>(st, 1, mA, mB, mC, M, N, K, ep, stream, trace_kind);
+  if (a_mn && b_mn) return launch_gemm_t<true, true>(st, 2, mA, mB, mC, M, N, K, ep, stream, trace_kind);
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 
@@ -245,20 +267,25 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   rc = check_ptrs("mlp_fwd", {X, A, a, B, b, U, Y, O});
   if (rc) return rc;
   if (R != nullptr && !aligned16(R)) return fail(MLP_EALIGN, "mlp_fwd: R is not 16-byte aligned");
-  if (t > 1) {
-    rc = check_ptrs("mlp_fwd (Zacc, needed when t > 1)", {Zacc});
+  if (t > 1 && slice >= 0) {
+    rc = check_ptrs("mlp_fwd (Zacc, needed for one-slice calls when t > 1)", {Zacc});
     if (rc) return rc;
   }
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int f = ffn / t;
   const int T = (int)tokens;
   const DropoutParams drop = make_dropout(p, seed, token_offset, h);
   if (R == nullptr) R = X;
+  // All slices in one call: each GEMM launch covers every slice.  F1 walks the
+  // column blocks A_0 .. A_{t-1} tile by tile, and F2's reduction loop walks the
+  // row blocks B_0 .. B_{t-1}, so the sum over slices of the partial products
+  // Y_i B_i happens in the TMEM accumulator.  One-slice calls reduce through Zacc.
+  if (slice < 0) t = 1;
+  const int f = ffn / t;
   const int i0 = slice < 0 ? 0 : slice;
-  const int i1 = slice < 0 ? t : slice + 1;
+  const int i1 = slice < 0 ? 1 : slice + 1;
   for (int i = i0; i < i1; ++i) {
     // F1: U_i = X A_i + a_i, Y_i = GeLU(U_i)          (M = T, N = f, K = h)
     EpiParams e1{};
@@ -297,18 +324,23 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   if (rc) return rc;
   rc = check_ptrs("mlp_bwd", {dO, X, A, B, U, Y, dZ, dU, dX, dA, da, dB, db});
   if (rc) return rc;
-  if (t > 1) {
-    rc = check_ptrs("mlp_bwd (dXacc, needed when t > 1)", {dXacc});
+  if (t > 1 && slice >= 0) {
+    rc = check_ptrs("mlp_bwd (dXacc, needed for one-slice calls when t > 1)", {dXacc});
     if (rc) return rc;
   }
   DeviceState* st = nullptr;
   rc = device_state(&st);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int f = ffn / t;
   const int T = (int)tokens;
   const DropoutParams drop = make_dropout(p, seed, token_offset, h);
-  if (slice <= 0) {
+  const bool first_call = slice <= 0;
+  // All slices in one call: B2, B3, B4 cover every slice's columns in one launch
+  // each, and B5's reduction loop walks A_0^T .. A_{t-1}^T so the sum over slices
+  // of dU_i A_i^T happens in the TMEM accumulator.  One-slice calls use dXacc.
+  if (slice < 0) t = 1;
+  const int f = ffn / t;
+  if (first_call) {
     // B1: dZ = dO * m / (1 - p), db += sum_tok dZ
     const int ts = trace_pre(s);
     k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dO, dZ, db, tokens, h, drop);
@@ -317,7 +349,7 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     if (rc) return rc;
   }
   const int i0 = slice < 0 ? 0 : slice;
-  const int i1 = slice < 0 ? t : slice + 1;
+  const int i1 = slice < 0 ? 1 : slice + 1;
   for (int i = i0; i < i1; ++i) {
     const int64_t c = (int64_t)i * f;
     // B2: dU_i = (dZ B_i^T) * GeLU'(U_i)                 (M = T, N = f, K = h)

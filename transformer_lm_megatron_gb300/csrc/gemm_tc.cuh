@@ -36,7 +36,12 @@ constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KB
 constexpr uint32_t kChunkBytes = 64 * kBK * 2;       // one 64 x BK box of an MN-major operand
 constexpr uint32_t kTmemCols = 2 * kBN;              // double-buffered accumulator
-constexpr size_t kGemmSmemBytes = (size_t)kStages * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+// fp32 outputs leave through TMA: each epilogue warp stages 32 rows x 32 columns
+// (4 KB, 128-byte swizzled) in one of two buffers and issues a bulk store/reduce.
+constexpr uint32_t kOutBoxBytes = 32 * 32 * 4;
+constexpr uint32_t kOutStageBytes = 4 * 2 * kOutBoxBytes;  // 4 warps x 2 buffers
+constexpr size_t kGemmSmemBytes =
+    (size_t)kStages * kStageBytes + kOutStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 enum EpiKind : int {
   kEpiGelu = 0,      // U = acc + bias (bf16), Y = GeLU(acc + bias) (bf16)
@@ -177,15 +182,17 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 }
 
 // A_MN / B_MN: operand stored MN-major (true) or K-major (false).
+// tmC: fp32 output map (box 32 x 32, 128-byte swizzle) used by kEpiF32Store / kEpiF32Add.
 template <bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, int M, int N,
-                   int K, EpiParams ep, int* status) {
+    k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sOut = sB + kStages * kBBytes;  // 1024-aligned
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kOutStageBytes);
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
@@ -215,9 +222,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
+  const bool tma_out = (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (tma_out) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -326,6 +335,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    uint8_t* my_out = sOut + (warp - 2) * 2 * kOutBoxBytes;
+    uint32_t n_out = 0;  // boxes this warp has issued
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < tile_end; tile += gridDim.x) {
@@ -343,7 +354,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c0, r);
         tmem_ld_wait();
-        if (row < M && n0 + c0 < N) epilogue_dispatch(ep, row, n0 + c0, r, N);
+        if (tma_out) {
+          // Warp-uniform: this warp's 32 rows x 32 columns go out as one TMA box;
+          // rows >= M and columns >= N are clipped by the tensor map.
+          if (n0 + c0 < N && m0 + quarter * 32 < M) {
+            uint8_t* box = my_out + (n_out & 1) * kOutBoxBytes;
+            if (lane == 0) bulk_wait_read<1>();  // the box issued two rounds ago has been read
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t off = lane * 128 + ((j ^ (lane & 7)) << 4);
+              *reinterpret_cast<uint4*>(box + off) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (ep.kind == kEpiF32Add)
+                tma_reduce_add_2d(&tmC, box, n0 + c0, m0 + quarter * 32);
+              else
+                tma_store_2d(&tmC, box, n0 + c0, m0 + quarter * 32);
+              bulk_commit();
+            }
+            ++n_out;
+          }
+        } else if (row < M && n0 + c0 < N) {
+          epilogue_dispatch(ep, row, n0 + c0, r, N);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -351,6 +387,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (lane == 0) bulk_wait_all();  // stores complete before the CTA (and its smem) goes away
   }
 
   tc_fence_before();
