@@ -153,6 +153,15 @@ int mlp_gelu_probe(const float* x, int64_t n, float* y, float* dy, void* stream)
  */
 int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream);
 
+/*
+ * mlp_set_cta_pair - choose the GEMM variant for later calls in this process:
+ * -1 (default) CTA pairs (clusters of two CTAs, 256 x 256 tiles, tcgen05
+ * cta_group::2) whenever a GEMM has more than 128 rows, else single CTAs
+ * (128 x 256 tiles); 0 always single CTAs; 1 always CTA pairs.  Results agree
+ * within the fp32 summation-order tolerance.  Returns MLP_OK or MLP_EINVAL.
+ */
+int mlp_set_cta_pair(int mode);
+
 /* mlp_launch_count - number of kernels this library has launched in this process. */
 uint64_t mlp_launch_count(void);
 

@@ -74,18 +74,27 @@ def test_tiny_workload_full_parity():
             assert np.all(to_f64(g_outs[j]["dZ"])[~keep] == 0)
 
 
+@pytest.fixture
+def cta_pair_mode(request):
+    mlp.mlp_set_cta_pair(request.param)
+    yield request.param
+    mlp.mlp_set_cta_pair(-1)
+
+
+@pytest.mark.parametrize("cta_pair_mode", [0, 1, -1], indirect=True, ids=["single", "pair", "auto"])
 @pytest.mark.parametrize("tokens,h,ffn,t", [
     (200, 136, 656, 2),     # ragged M, N and K tails (none a multiple of the 128/256/64 tiles)
     (1, 64, 128, 1),        # a single token
     (130, 8, 64, 4),        # h = 8: one partial k-block, f = 16
     (384, 320, 1280, 1),    # several M tiles, N tail of 64
+    (520, 264, 1040, 2),    # M tail of 8 rows past two CTA-pair tiles
 ])
-def test_ragged_shapes_full_parity(tokens, h, ffn, t):
+def test_ragged_shapes_full_parity(tokens, h, ffn, t, cta_pair_mode):
     s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2, p=0.1)
     w_dev, mbs_dev, w64, mbs64 = make_case(s)
     g_outs, g_grads = run_gpu(s, w_dev, mbs_dev)
     r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
-    compare_full(s, g_outs, g_grads, r_outs, r_grads)
+    compare_full(s, g_outs, g_grads, r_outs, r_grads, label=f"pair mode {cta_pair_mode}")
 
 
 @pytest.mark.parametrize("t", [2, 4, 8])

@@ -89,8 +89,12 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;
-  bool gemm_attr[3] = {false, false, false};
+  bool gemm_attr[8] = {};   // per GEMM instantiation: dynamic smem attribute set
+  int max_pairs[8] = {};    // per CTA-pair instantiation: co-resident clusters of two
 };
+
+// -1: CTA pairs whenever a tile has more than 128 rows; 0: single CTAs; 1: CTA pairs.
+std::atomic<int> g_pair_mode{-1};
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -178,22 +182,64 @@ int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int
   return make_map(m, base, k, mn, ld, kBK, tile_mn);
 }
 
-template <bool AM, bool BM>
-int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
-                  int M, int N, int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
-  auto kern = k_gemm_bf16_tc<AM, BM>;
+template <bool AM, bool BM, bool PAIR>
+int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, int M, int N,
+                  int K, const EpiParams& ep, int raster_n_fast, cudaStream_t stream, int trace_kind) {
+  using Cfg = GemmCfg<PAIR>;
+  auto kern = k_gemm_bf16_tc<AM, BM, PAIR>;
+  const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0);
   if (!st->gemm_attr[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemBytes);
     if (e != cudaSuccess) return fail(MLP_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+    if (PAIR) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+      cudaLaunchConfig_t qc = {};
+      qc.gridDim = dim3(2 * (unsigned)st->sms, 1, 1);
+      qc.blockDim = dim3(kGemmThreads, 1, 1);
+      qc.dynamicSmemBytes = Cfg::kSmemBytes;
+      cudaLaunchAttribute qa[1];
+      qa[0].id = cudaLaunchAttributeClusterDimension;
+      qa[0].val.clusterDim.x = 2;
+      qa[0].val.clusterDim.y = 1;
+      qa[0].val.clusterDim.z = 1;
+      qc.attrs = qa;
+      qc.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &qc);
+      if (e != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = st->sms / 2;
+      }
+      st->max_pairs[slot] = n;
+    }
     st->gemm_attr[slot] = true;
   }
-  const int64_t tiles = (int64_t)((M + kBM - 1) / kBM) * ((N + kBN - 1) / kBN);
-  const int grid = (int)(tiles < st->sms ? tiles : st->sms);
+  const int64_t tiles = (int64_t)((M + Cfg::kTileM - 1) / Cfg::kTileM) * ((N + kBN - 1) / kBN);
   const int ts = trace_pre(stream);
-  kern<<<grid, kGemmThreads, kGemmSmemBytes, stream>>>(mA, mB, mC, M, N, K, ep, st->status);
+  cudaError_t e;
+  if (PAIR) {
+    const int pairs = (int)(tiles < st->max_pairs[slot] ? tiles : st->max_pairs[slot]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
+    cfg.blockDim = dim3(kGemmThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, M, N, K, ep, raster_n_fast, st->status);
+  } else {
+    const int grid = (int)(tiles < st->sms ? tiles : st->sms);
+    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, M, N, K, ep, raster_n_fast, st->status);
+    e = cudaGetLastError();
+  }
   trace_post(ts, stream, trace_kind, M, N, K);
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLP_ECUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return MLP_OK;
 }
@@ -201,10 +247,12 @@ int launch_gemm_t(DeviceState* st, int slot, const CUtensorMap& mA, const CUtens
 // D[M, N] = A(M x K) B(K x N) with the given operand layouts and epilogue.
 int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, bool b_mn, int64_t ldb, int M, int N,
          int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+  const int mode = g_pair_mode.load(std::memory_order_relaxed);
+  const bool pair = mode == 1 || (mode < 0 && M > kBM);
   CUtensorMap mA, mB, mC;
   int rc = operand_map(&mA, a, a_mn, M, K, lda, kBM);
   if (rc) return rc;
-  rc = operand_map(&mB, b, b_mn, N, K, ldb, kBN);
+  rc = operand_map(&mB, b, b_mn, N, K, ldb, pair ? GemmCfg<true>::kBLoadN : GemmCfg<false>::kBLoadN);
   if (rc) return rc;
   if (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add) {
     rc = make_out_map(&mC, ep.g_out, N, M, ep.ld);
@@ -212,9 +260,17 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
   } else {
     memset(&mC, 0, sizeof(mC));
   }
-  if (!a_mn && b_mn) return launch_gemm_t<false, true>(st, 0, mA, mB, mC, M, N, K, ep, stream, trace_kind);
-  if (!a_mn && !b_mn) return launch_gemm_t<false, false>(st, 1, mA, mB, mC, M, N, K, ep, stream, trace_kind);
-  if (a_mn && b_mn) return launch_gemm_t<true, true>(st, 2, mA, mB, mC, M, N, K, ep, stream, trace_kind);
+  // Visit tiles so that the operand re-read across the sweep is the smaller one.
+  const int raster_n_fast = M > N ? 1 : 0;
+  if (!a_mn && b_mn)
+    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind)
+                : launch_gemm_t<false, true, false>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind);
+  if (!a_mn && !b_mn)
+    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind)
+                : launch_gemm_t<false, false, false>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind);
+  if (a_mn && b_mn)
+    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind)
+                : launch_gemm_t<true, true, false>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind);
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 
@@ -474,6 +530,12 @@ int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream) {
 }
 
 uint64_t mlp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int mlp_set_cta_pair(int mode) {
+  if (mode < -1 || mode > 1) return fail(MLP_EINVAL, "mlp_set_cta_pair: mode %d not in {-1, 0, 1}", mode);
+  g_pair_mode.store(mode, std::memory_order_relaxed);
+  return MLP_OK;
+}
 
 int mlp_trace_begin(int capacity) {
   if (capacity <= 0 || capacity > (1 << 20)) return fail(MLP_EINVAL, "mlp_trace_begin: capacity %d out of range", capacity);

@@ -4,14 +4,21 @@
 //
 // Operands live row-major in HBM; each may be K-major (k contiguous) or MN-major
 // (m or n contiguous), so the six contractions of the MLP block's forward and
-// backward never materialise a transpose.  Tiles are BM x BN = 128 x 256 with
-// BK = 64 (one 128-byte swizzle atom of bf16 along the contiguous dimension).
+// backward never materialise a transpose.  Each CTA owns 128 x 256 of D per
+// tile, with BK = 64 (one 128-byte swizzle atom of bf16 along the contiguous
+// dimension).  Two variants:
+//   single CTA  tcgen05.mma.cta_group::1, M = 128, N = 256; 4-stage ring of 48 KB.
+//   CTA pair    a cluster of two CTAs computes a 256 x 256 tile with
+//               tcgen05.mma.cta_group::2 issued by the even CTA: each CTA loads
+//               its own 128 rows of A and its half (128) of B's columns, so per
+//               SM the B traffic (smem and L2) halves; 6-stage ring of 32 KB.
 //
 // Warp roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: loads A/B k-blocks into a STAGES-deep smem ring.
-//   warp 1      TMEM owner and MMA issuer: one thread issues tcgen05.mma; the
-//               accumulator is double-buffered (2 x BN fp32 columns of TMEM) so
-//               the epilogue of tile j overlaps the main loop of tile j+1.
+//   warp 0      TMA producer: loads A/B k-blocks into the smem ring.
+//   warp 1      TMEM owner and (even CTA) MMA issuer: one thread issues
+//               tcgen05.mma; the accumulator is double-buffered (2 x 256 fp32
+//               columns of TMEM) so the epilogue of tile j overlaps the main
+//               loop of tile j+1.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lane
 //               quarter w % 4, i.e. tile rows 32*(w%4) .. +31), fused element-wise
 //               work, vectorised global stores.
@@ -26,22 +33,28 @@
 
 namespace gbmlp {
 
-constexpr int kBM = 128;
-constexpr int kBN = 256;
+constexpr int kBM = 128;   // rows of D per CTA per tile
+constexpr int kBN = 256;   // columns of D per tile (the MMA's N)
 constexpr int kBK = 64;
-constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;
-constexpr uint32_t kABytes = kBM * kBK * 2;          // 16 KB
-constexpr uint32_t kBBytes = kBN * kBK * 2;          // 32 KB
-constexpr uint32_t kStageBytes = kABytes + kBBytes;  // 48 KB
-constexpr uint32_t kChunkBytes = 64 * kBK * 2;       // one 64 x BK box of an MN-major operand
-constexpr uint32_t kTmemCols = 2 * kBN;              // double-buffered accumulator
+constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KB
+constexpr uint32_t kChunkBytes = 64 * kBK * 2;  // one 64 x BK box of an MN-major operand
+constexpr uint32_t kTmemCols = 2 * kBN;         // double-buffered accumulator
 // fp32 outputs leave through TMA: each epilogue warp stages 32 rows x 32 columns
 // (4 KB, 128-byte swizzled) in one of two buffers and issues a bulk store/reduce.
 constexpr uint32_t kOutBoxBytes = 32 * 32 * 4;
 constexpr uint32_t kOutStageBytes = 4 * 2 * kOutBoxBytes;  // 4 warps x 2 buffers
-constexpr size_t kGemmSmemBytes =
-    (size_t)kStages * kStageBytes + kOutStageBytes + 1024 /*align*/ + 256 /*barriers*/;
+
+template <bool PAIR>
+struct GemmCfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBLoadN = PAIR ? kBN / 2 : kBN;      // B rows (N) this CTA loads per stage
+  static constexpr int kTileM = PAIR ? 2 * kBM : kBM;       // rows of D per tile
+  static constexpr uint32_t kBBytes = kBLoadN * kBK * 2;
+  static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kOutStageBytes + 1024 /*align*/ + 256;
+};
+static_assert(GemmCfg<true>::kSmemBytes <= 232448 && GemmCfg<false>::kSmemBytes <= 232448, "smem budget");
 
 enum EpiKind : int {
   kEpiGelu = 0,      // U = acc + bias (bf16), Y = GeLU(acc + bias) (bf16)
@@ -182,16 +195,22 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 }
 
 // A_MN / B_MN: operand stored MN-major (true) or K-major (false).
+// PAIR: launched as clusters of two CTAs (see the file comment).
 // tmC: fp32 output map (box 32 x 32, 128-byte swizzle) used by kEpiF32Store / kEpiF32Add.
-template <bool A_MN, bool B_MN>
+// raster_n_fast: tiles are visited with N varying fastest (else M fastest), so that
+// the operand re-read across the sweep is the smaller one and stays in L2.
+template <bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int* status) {
+                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int raster_n_fast,
+                   int* status) {
+  using Cfg = GemmCfg<PAIR>;
+  constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint8_t* sOut = sB + kStages * kBBytes;  // 1024-aligned
+  uint8_t* sOut = sB + kStages * Cfg::kBBytes;  // 1024-aligned
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kOutStageBytes);
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
@@ -201,7 +220,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int num_m = (M + kBM - 1) / kBM;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;     // 0 = the CTA that issues the MMAs
+  const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int num_groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int num_m = (M + Cfg::kTileM - 1) / Cfg::kTileM;
   const int num_n = (N + kBN - 1) / kBN;
   const int num_tiles = num_m * num_n;
   const int num_kb = (K + kBK - 1) / kBK;
@@ -217,7 +239,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(mma_done, 1);
     fence_mbar_init();
@@ -229,14 +251,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (tma_out) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(tmem_slot, kTmemCols);
+    tmem_relinquish<PAIR>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) {
+    // both CTAs' barriers are initialised before either CTA signals the other's;
+    // the skip decision is shared so both CTAs walk the same tiles
+    cluster_sync();
+  }
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int tile_end = s_skip ? 0 : num_tiles;
+  int skip = s_skip;
+  if constexpr (PAIR) {
+    int* peer_skip = static_cast<int*>(__cluster_map_shared_rank(static_cast<void*>(&s_skip), rank ^ 1u));
+    skip |= *reinterpret_cast<volatile int*>(peer_skip);
+    cluster_sync();  // the peer has read s_skip before anything else touches it
+  }
+  const int tile_end = skip ? 0 : num_tiles;
+
+  auto tile_origin = [&](int tile, int& m0, int& n0) {
+    int mb, nb;
+    if (raster_n_fast) {
+      nb = tile % num_n;
+      mb = tile / num_n;
+    } else {
+      mb = tile % num_m;
+      nb = tile / num_m;
+    }
+    m0 = mb * Cfg::kTileM + (int)rank * kBM;  // this CTA's first row
+    n0 = nb * kBN;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -247,9 +293,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tile_end && ok; tile += gridDim.x) {
-        const int m0 = (tile % num_m) * kBM;
-        const int n0 = (tile / num_m) * kBN;
+      for (int tile = group; tile < tile_end && ok; tile += num_groups) {
+        int m0, n0;
+        tile_origin(tile, m0, n0);
+        const int b_n0 = n0 + (PAIR ? (int)rank * Cfg::kBLoadN : 0);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             record_status(status, kStatusTimeout, 1);
@@ -257,20 +304,41 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             break;
           }
           const int k0 = kb * kBK;
-          mbar_arrive_expect_tx(&full[stage], kStageBytes);
           uint8_t* a_dst = sA + stage * kABytes;
-          uint8_t* b_dst = sB + stage * kBBytes;
-          if constexpr (A_MN) {
+          uint8_t* b_dst = sB + stage * Cfg::kBBytes;
+          if constexpr (PAIR) {
+            // both CTAs' copies complete on the even CTA's barrier, which expects both
+            const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
+            if constexpr (A_MN) {
 #pragma unroll
-            for (int j = 0; j < kBM / 64; ++j) tma_load_2d(a_dst + j * kChunkBytes, &tmA, &full[stage], m0 + 64 * j, k0);
-          } else {
-            tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
-          }
-          if constexpr (B_MN) {
+              for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(a_dst + j * kChunkBytes, &tmA, bar, m0 + 64 * j, k0);
+            } else {
+              tma_load_2d_pair(a_dst, &tmA, bar, k0, m0);
+            }
+            if constexpr (B_MN) {
 #pragma unroll
-            for (int j = 0; j < kBN / 64; ++j) tma_load_2d(b_dst + j * kChunkBytes, &tmB, &full[stage], n0 + 64 * j, k0);
+              for (int j = 0; j < Cfg::kBLoadN / 64; ++j)
+                tma_load_2d_pair(b_dst + j * kChunkBytes, &tmB, bar, b_n0 + 64 * j, k0);
+            } else {
+              tma_load_2d_pair(b_dst, &tmB, bar, k0, b_n0);
+            }
           } else {
-            tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
+            mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+            if constexpr (A_MN) {
+#pragma unroll
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_2d(a_dst + j * kChunkBytes, &tmA, &full[stage], m0 + 64 * j, k0);
+            } else {
+              tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+            }
+            if constexpr (B_MN) {
+#pragma unroll
+              for (int j = 0; j < Cfg::kBLoadN / 64; ++j)
+                tma_load_2d(b_dst + j * kChunkBytes, &tmB, &full[stage], b_n0 + 64 * j, k0);
+            } else {
+              tma_load_2d(b_dst, &tmB, &full[stage], k0, b_n0);
+            }
           }
           ++issued[stage];
           if (++stage == kStages) {
@@ -279,56 +347,79 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
         }
       }
-      // Drain: every copy this thread issued has landed before the CTA may exit.
-      for (int s = 0; s < kStages; ++s) {
-        if (issued[s] > 0 && !mbar_wait(&full[s], (issued[s] - 1) & 1)) record_status(status, kStatusTimeout, 2);
+      // Drain: every copy this CTA issued has landed before the CTA may exit.
+      if (!PAIR || rank == 0) {
+        for (int s = 0; s < kStages; ++s) {
+          if (issued[s] > 0 && !(PAIR ? mbar_wait_cluster(&full[s], (issued[s] - 1) & 1)
+                                      : mbar_wait(&full[s], (issued[s] - 1) & 1)))
+            record_status(status, kStatusTimeout, 2);
+        }
+      } else if (!ok) {
+        // the odd CTA's copies complete on the even CTA's barrier; after a failure
+        // give any copy still in flight time to land (bounded)
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(10000);
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && rank == 0) {
       // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = make_idesc_bf16(kBM, kBN, A_MN, B_MN);
+      constexpr uint32_t idesc = make_idesc_bf16(PAIR ? 2 * kBM : kBM, kBN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < tile_end && ok; tile += gridDim.x) {
-        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1)) {
+      for (int tile = group; tile < tile_end && ok; tile += num_groups) {
+        if (!(PAIR ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1) : mbar_wait(&acc_empty[acc], acc_phase ^ 1))) {
           record_status(status, kStatusTimeout, 3);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
         for (int kb = 0; kb < num_kb; ++kb) {
-          if (!mbar_wait(&full[stage], phase)) {
+          if (!(PAIR ? mbar_wait_cluster(&full[stage], phase) : mbar_wait(&full[stage], phase))) {
             record_status(status, kStatusTimeout, 4);
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * kABytes);
-          const uint32_t b_base = smem_u32(sB + stage * kBBytes);
+          const uint32_t b_base = smem_u32(sB + stage * Cfg::kBBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
             const uint64_t adesc = A_MN ? make_sdesc_sw128(a_base + kk * 2048, kChunkBytes, 1024)
                                         : make_sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc = B_MN ? make_sdesc_sw128(b_base + kk * 2048, kChunkBytes, 1024)
                                         : make_sdesc_sw128(b_base + kk * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            if constexpr (PAIR)
+              umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          umma_commit(&empty[stage]);  // the smem stage is free once these MMAs have read it
+          // the smem stage (of both CTAs) is free once these MMAs have read it
+          if constexpr (PAIR)
+            umma_commit_pair(&empty[stage], 0x3);
+          else
+            umma_commit(&empty[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&acc_full[acc]);  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue warps (of both CTAs)
+        if constexpr (PAIR)
+          umma_commit_pair(&acc_full[acc], 0x3);
+        else
+          umma_commit(&acc_full[acc]);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
-      umma_commit(mma_done);
+      if constexpr (PAIR)
+        umma_commit_pair(mma_done, 0x1);
+      else
+        umma_commit(mma_done);
       if (!mbar_wait(mma_done, 0)) record_status(status, kStatusTimeout, 5);
     }
   } else {
@@ -339,10 +430,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t n_out = 0;  // boxes this warp has issued
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < tile_end; tile += gridDim.x) {
-      const int m0 = (tile % num_m) * kBM;
-      const int n0 = (tile / num_m) * kBN;
-      if (!mbar_wait(&acc_full[acc], acc_phase)) {
+    for (int tile = group; tile < tile_end; tile += num_groups) {
+      int m0, n0;
+      tile_origin(tile, m0, n0);
+      if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
       }
@@ -383,7 +474,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[acc]);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&acc_empty[acc]), 0));
+        else
+          mbar_arrive(&acc_empty[acc]);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -392,9 +488,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (PAIR) cluster_sync();  // the even CTA's MMAs no longer read the odd CTA's smem / TMEM
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc<PAIR>(tmem_base, kTmemCols);
   }
 }
 

@@ -40,6 +40,7 @@ _SIGNATURES = {
     "mlp_gelu_probe": (_i32, [_vp, _i64, _vp, _vp, _vp]),
     "mlp_wait_timeout_probe": (_i32, [_u64, _vp]),
     "mlp_launch_count": (_u64, []),
+    "mlp_set_cta_pair": (_i32, [_i32]),
     "mlp_trace_begin": (_i32, [_i32]),
     "mlp_trace_end": (_i32, [_i32, _vp, _vp, _vp]),
 }
@@ -130,6 +131,10 @@ def mlp_wait_timeout_probe(limit_ns, stream=None):
 
 def mlp_launch_count() -> int:
     return int(load().mlp_launch_count())
+
+
+def mlp_set_cta_pair(mode: int):
+    _check(load().mlp_set_cta_pair(mode))
 
 
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
