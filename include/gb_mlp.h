@@ -183,6 +183,35 @@ int mlp_trace_begin(int capacity);
  */
 int mlp_trace_end(int max_entries, int* kinds, int64_t* mnk, float* ms);
 
+/*
+ * mlp_fwd_static_scratch - mlp_fwd for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is an integration variant.
+ *
+ * One-slice forward calls (slice = i with t > 1) sum the row-split partial
+ * products of successive calls in an fp32 [tokens, h] workspace, which mlp_fwd
+ * takes from the caller (Zacc).  A plugin that runs inside a host application
+ * owning all device memory through its own pool, or a serving loop that must not
+ * allocate once it runs (cudaMalloc / cudaFree can synchronise the device), has no
+ * such buffer to give.  This entry point takes the same arguments as mlp_fwd
+ * without Zacc and uses a fixed 16 MiB array in the library's own device memory
+ * instead; every GPU that loads the library holds that array until the process
+ * exits.  It allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *
+ *   - tokens * h must not exceed 4,194,304 (16 MiB of fp32), else MLP_EINVAL
+ *     with a message naming the limit; the limit applies to every call.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.  The
+ *     slice-0 call overwrites it (nothing needs clearing), later slices add to it,
+ *     and the last slice reads it.  Calls whose work overlaps on the GPU (other
+ *     streams, other threads, other sequences of one-slice calls) race on it.
+ * Everything else (arguments, layouts, results) is as for mlp_fwd.
+ */
+int mlp_fwd_static_scratch(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed,
+                           uint64_t token_offset, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* a,
+                           const mlp_bf16* B, const mlp_bf16* b, const mlp_bf16* R, mlp_bf16* U, mlp_bf16* Y,
+                           mlp_bf16* O, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

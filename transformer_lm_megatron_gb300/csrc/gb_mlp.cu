@@ -313,6 +313,10 @@ int launch_check(const char* what) {
 
 }  // namespace
 
+namespace gbmlp {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace gbmlp
+
 extern "C" {
 
 int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,

@@ -41,6 +41,7 @@ _SIGNATURES = {
     "mlp_wait_timeout_probe": (_i32, [_u64, _vp]),
     "mlp_launch_count": (_u64, []),
     "mlp_set_cta_pair": (_i32, [_i32]),
+    "mlp_fwd_static_scratch": (_i32, [_i32, _i32, _i32, _i32, _i64, _f32, _u64, _u64] + [_vp] * 6 + [_vp, _vp, _vp, _vp]),
     "mlp_trace_begin": (_i32, [_i32]),
     "mlp_trace_end": (_i32, [_i32, _vp, _vp, _vp]),
 }
@@ -107,6 +108,14 @@ def mlp_bwd(h, ffn, t, slice_, tokens, p, seed, token_offset, residual_grad, dO,
     _check(load().mlp_bwd(h, ffn, t, slice_, tokens, p, seed, token_offset, int(residual_grad), _ptr(dO), _ptr(X),
                           _ptr(A), _ptr(B), _ptr(U), _ptr(Y), _ptr(dZ), _ptr(dU), _ptr(dXacc), _ptr(dX), _ptr(dA),
                           _ptr(da), _ptr(dB), _ptr(db), _stream(stream)))
+
+
+def mlp_fwd_static_scratch(h, ffn, t, slice_, tokens, p, seed, token_offset, X, A, a, B, b, R, U, Y, O,
+                           stream=None):
+    """mlp_fwd for callers that cannot allocate: the fp32 slice workspace is the
+    library's own fixed 16 MiB array (tokens * h <= 4,194,304); see the header."""
+    _check(load().mlp_fwd_static_scratch(h, ffn, t, slice_, tokens, p, seed, token_offset, _ptr(X), _ptr(A), _ptr(a),
+                                         _ptr(B), _ptr(b), _ptr(R), _ptr(U), _ptr(Y), _ptr(O), _stream(stream)))
 
 
 def grad_accum_reset(h, ffn, dA, da, dB, db, stream=None):
