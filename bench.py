@@ -182,10 +182,17 @@ def run_ours(args, wl, rank, world, dist):
     buf = mlp.BlockBuffers(wl.tokens, wl.h, wl.ffn, wl.t, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    def reset():
+        mlp.grad_accum_reset(wl.h, wl.ffn, buf.dA, buf.da, buf.dB, buf.db, stream=stream)
+
     def step():
+        if args.reset_each_step:
+            reset()
+        # one optimizer step's worth of micro-batches: the first writes the fp32
+        # gradients (accumulate = 0), the others add to them
         for j, (X, dO) in enumerate(mbs):
             mlp.block_step(wl, weights, X, dO, buf, token_offset=j * wl.tokens, slice_mode=args.slice_mode,
-                           stream=stream)
+                           stream=stream, accumulate=(j > 0 or args.reset_each_step))
 
     mlp.grad_accum_reset(wl.h, wl.ffn, buf.dA, buf.da, buf.dB, buf.db, stream=stream)
     for _ in range(args.warmup):
@@ -244,7 +251,7 @@ def run_ours(args, wl, rank, world, dist):
                 dX_in[j].copy_(hX[j], non_blocking=True)
                 ddO_in[j].copy_(hdO[j], non_blocking=True)
                 mlp.block_step(wl, weights, dX_in[j], ddO_in[j], buf, token_offset=j * wl.tokens,
-                               slice_mode=args.slice_mode, stream=stream)
+                               slice_mode=args.slice_mode, stream=stream, accumulate=(j > 0 or args.reset_each_step))
                 hO[j].copy_(buf.O, non_blocking=True)
                 hdX[j].copy_(buf.dX, non_blocking=True)
 
@@ -293,7 +300,9 @@ def run_ours(args, wl, rank, world, dist):
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, all slices on-device",
                    "l2": "inputs larger than L2 (bf16 weights %.1f GB, fp32 gradients %.1f GB)"
                          % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9),
-                   "grad_accum_reset": "outside the timed region"},
+                   "grad_init": ("grad_accum_reset + every micro-batch adds (inside the timed region)"
+                                 if args.reset_each_step else
+                                 "first micro-batch of each step writes dA/da/dB/db, later ones add; no reset pass")},
         "gpu_launches": n_launch,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -315,6 +324,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", dest="trace", action="store_false")
+    ap.add_argument("--reset-each-step", action="store_true",
+                    help="time grad_accum_reset + all micro-batches adding, instead of the first writing")
     args = ap.parse_args()
 
     from transformer_lm_megatron_gb300 import inputs as gin

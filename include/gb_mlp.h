@@ -90,8 +90,12 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
             const mlp_bf16* R, mlp_bf16* U, mlp_bf16* Y, float* Zacc, mlp_bf16* O, void* stream);
 
 /*
- * mlp_bwd - backward of one micro-batch; weight and bias gradients ACCUMULATE
- * (+=) into the fp32 dA, da, dB, db (gradient accumulation over micro-batches).
+ * mlp_bwd - backward of one micro-batch.  Weight and bias gradients go to the
+ * fp32 dA, da, dB, db: with accumulate = 1 they are ADDED (+=), which sums the
+ * micro-batches of a step (gradient accumulation); with accumulate = 0 they
+ * OVERWRITE the accumulators, which is how the first micro-batch of a step starts
+ * the sum without a separate grad_accum_reset (the two agree bit for bit:
+ * 0 + x = x).
  *
  *   slice == -1 or slice == i as for mlp_fwd (order 0 .. t-1).  The call with
  *   slice 0 (or -1) computes dZ and db; the call with slice t-1 (or -1) writes
@@ -99,6 +103,10 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
  *   fp32 accumulator on chip and dXacc is not used.
  *   residual_grad  1: dX = dO + sum_i dU_i A_i^T (the residual R was X);
  *                  0: dX = sum_i dU_i A_i^T.
+ *   accumulate     1: dA, da, dB, db += this micro-batch's gradients;
+ *                  0: dA, da, dB, db  = this micro-batch's gradients.  With
+ *                     one-slice calls each slice writes its own columns of dA
+ *                     and da and rows of dB; db is written by the slice-0 call.
  *   dO     [tokens, h]  upstream gradient of O.
  *   X, A, B           as passed to mlp_fwd; U, Y as written by mlp_fwd.
  *   dZ     [tokens, h]  workspace/output: gradient after dropout (bf16).
@@ -106,11 +114,11 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
  *   dXacc  [tokens, h] fp32 workspace for the sum over slices of one-slice
  *                        calls; may be NULL when t == 1 or slice == -1.
  *   dX     [tokens, h]  output (overwritten).
- *   dA, da, dB, db    fp32 gradient accumulators (+=).
+ *   dA, da, dB, db    fp32 gradient accumulators (+= or =, see accumulate).
  * Returns MLP_OK or an error code.
  */
 int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,
-            int residual_grad, const mlp_bf16* dO, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
+            int residual_grad, int accumulate, const mlp_bf16* dO, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
             const mlp_bf16* U, const mlp_bf16* Y, mlp_bf16* dZ, mlp_bf16* dU, float* dXacc, mlp_bf16* dX,
             float* dA, float* da, float* dB, float* db, void* stream);
 

@@ -75,16 +75,16 @@ def test_fwd_rejects_bad_arguments(lib, kw, code):
 
 def test_bwd_rejects_bad_arguments(lib):
     g = GOOD
-    args = [64, 256, 2, -1, 16, 0.1, 1234, 0, 1] + [g] * 8 + [g, g] + [g] * 4 + [None]
+    args = [64, 256, 2, -1, 16, 0.1, 1234, 0, 1, 1] + [g] * 8 + [g, g] + [g] * 4 + [None]
     bad = list(args)
     bad[0] = 20
     assert lib.mlp_bwd(*bad) == mlp.MLP_EINVAL
     bad = list(args)
     bad[3] = 0                                       # one-slice call with t > 1 ...
-    bad[17] = None                                   # ... needs the dXacc workspace
+    bad[18] = None                                   # ... needs the dXacc workspace
     assert lib.mlp_bwd(*bad) == mlp.MLP_EINVAL
     bad = list(args)
-    bad[9] = g + 4                                   # dO misaligned
+    bad[10] = g + 4                                  # dO misaligned
     assert lib.mlp_bwd(*bad) == mlp.MLP_EALIGN
 
 

@@ -163,6 +163,24 @@ def test_exact_invariants():
     assert torch.equal(outs0[0]["O"], X.cpu())
 
 
+@pytest.mark.parametrize("mode", ["all", "each"])
+def test_first_microbatch_overwrite_equals_reset_then_accumulate(mode):
+    """accumulate = 0 on the first micro-batch (accumulators left holding NaN)
+    gives bit for bit what grad_accum_reset + accumulate = 1 gives."""
+    s = Shape(tokens=200, h=256, ffn=1024, t=4, k=3)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    _, g_ref = run_gpu(s, w_dev, mbs_dev, slice_mode=mode)
+    buf = mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t)
+    for k in ("dA", "da", "dB", "db"):
+        getattr(buf, k).fill_(float("nan"))
+    _, g_new = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, buf=buf, reset=False, first_overwrites=True)
+    for k in g_ref:
+        assert torch.equal(g_new[k], g_ref[k]), k
+    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
+    for k in ("dA", "da", "dB", "db"):
+        assert rel_err(to_f64(g_new[k]), r_grads[k]) <= F32_TOL, k
+
+
 def test_bounded_wait_reports_timeout():
     assert mlp.mlp_sync_status() == mlp.MLP_OK
     mlp.mlp_wait_timeout_probe(1000000)   # 1 ms

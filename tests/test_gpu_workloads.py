@@ -42,16 +42,23 @@ def test_small_workload_full_parity():
     compare_full(s, g_outs, g_grads, r_outs, r_grads, label="small")
 
 
-def _sampled_check(wl, slice_mode, n_rows=24, n_entries=96, seed=0):
+def _sampled_check(wl, slice_mode, n_rows=24, n_entries=96, seed=0, first_overwrites=False):
     """Runs the workload on the GPU (inputs drawn on the GPU with the seeded
-    generators) and checks sampled outputs against the oracle."""
+    generators) and checks sampled outputs against the oracle.  first_overwrites:
+    no reset; the first micro-batch overwrites the accumulators (which start as
+    NaN), as the benchmark runs it."""
     dev = torch.device("cuda")
     w = gin.make_weights(wl.h, wl.ffn, device=dev)
     mbs = [gin.make_microbatch(wl.tokens, wl.h, j, device=dev) for j in range(wl.k)]
     buf = mlp.BlockBuffers(wl.tokens, wl.h, wl.ffn, wl.t, device=dev)
-    mlp.grad_accum_reset(wl.h, wl.ffn, buf.dA, buf.da, buf.dB, buf.db)
+    if first_overwrites:
+        for k in ("dA", "da", "dB", "db"):
+            getattr(buf, k).fill_(float("nan"))
+    else:
+        mlp.grad_accum_reset(wl.h, wl.ffn, buf.dA, buf.da, buf.dB, buf.db)
     for j, (X, dO) in enumerate(mbs):
-        mlp.block_step(wl, w, X, dO, buf, token_offset=j * wl.tokens, slice_mode=slice_mode)
+        mlp.block_step(wl, w, X, dO, buf, token_offset=j * wl.tokens, slice_mode=slice_mode,
+                       accumulate=not (first_overwrites and j == 0))
     torch.cuda.synchronize()
     assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
 
@@ -113,8 +120,9 @@ def test_mid_workload_sampled_parity():
 
 
 def test_mtnlg_layer_sampled_parity():
-    """2048 tokens, h 20480, ffn 81920, t 8: all slices per call, as benchmarked."""
-    _sampled_check(gin.WORKLOADS["mtnlg"], "all", n_rows=16, n_entries=64)
+    """2048 tokens, h 20480, ffn 81920, t 8: all slices per call, the first (only)
+    micro-batch writing the gradients, as benchmarked."""
+    _sampled_check(gin.WORKLOADS["mtnlg"], "all", n_rows=16, n_entries=64, first_overwrites=True)
 
 
 def test_mtnlg_layer_one_slice_calls_sampled_parity():
@@ -123,7 +131,7 @@ def test_mtnlg_layer_one_slice_calls_sampled_parity():
     _sampled_check(gin.WORKLOADS["mtnlg"], "each", n_rows=8, n_entries=32, seed=1)
 
 
-@pytest.mark.parametrize("name", ["sweep4"])
-def test_accumulation_sweep_sampled_parity(name):
+@pytest.mark.parametrize("name,first_overwrites", [("sweep4", False), ("sweep16", True)])
+def test_accumulation_sweep_sampled_parity(name, first_overwrites):
     """h 8192, ffn 32768, t 4, one slice per call in turn, micro-batches accumulated."""
-    _sampled_check(gin.WORKLOADS[name], "each")
+    _sampled_check(gin.WORKLOADS[name], "each", n_rows=12, n_entries=48, first_overwrites=first_overwrites)

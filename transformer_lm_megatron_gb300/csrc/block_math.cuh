@@ -18,19 +18,36 @@ namespace gbmlp {
 constexpr float kSqrt2OverPi = 0.7978845608028654f;
 constexpr float kGeluCubic = 0.044715f;
 
-__device__ __forceinline__ float gelu_f(float x) {
-  const float s = kSqrt2OverPi * (x + kGeluCubic * x * x * x);
-  return 0.5f * x * (1.0f + tanhf(s));
+// 1 / y with the hardware reciprocal approximation (about 1 ulp); 1/inf = 0.
+__device__ __forceinline__ float rcp_approx(float y) {
+  float r;
+  asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(y));
+  return r;
 }
 
-// For |x| >= 30 the fp32 result is already exactly 1 (x > 0) or 0 (x < 0); the
-// clamp keeps x*x finite so that (1 - th*th) * ds never becomes 0 * inf.
+// The tanh form rewritten without cancellation: 0.5 x (1 + tanh(s)) = x * sigmoid(2 s)
+// = x / (1 + exp(-2 s)), s = sqrt(2/pi) (x + 0.044715 x^3).  Beyond x = +-30 the
+// sigmoid factor is 0 or 1 in fp32, so s is evaluated at the clamped x and the
+// exponent is capped at 80 (the result there is below 1e-33 in magnitude).
+__device__ __forceinline__ float gelu_f(float x) {
+  const float xn = fmaxf(x, -30.0f);
+  const float xc = fminf(xn, 30.0f);
+  const float s = kSqrt2OverPi * fmaf(kGeluCubic * xc, xc * xc, xc);
+  const float e = __expf(fminf(-2.0f * s, 80.0f));
+  return xn * rcp_approx(1.0f + e);
+}
+
+// d/dx [x * sig(2 s)] = sig(2 s) + 2 x s'(x) sig(2 s) (1 - sig(2 s)), with
+// sig(2 s) = r = 1 / (1 + e), 1 - sig(2 s) = e r, e = exp(-2 s), and
+// s'(x) = sqrt(2/pi) (1 + 3 * 0.044715 x^2).  Same clamps as gelu_f.
 __device__ __forceinline__ float gelu_prime_f(float x) {
   x = fminf(fmaxf(x, -30.0f), 30.0f);
-  const float s = kSqrt2OverPi * (x + kGeluCubic * x * x * x);
-  const float th = tanhf(s);
-  const float ds = kSqrt2OverPi * (1.0f + 3.0f * kGeluCubic * x * x);
-  return 0.5f * (1.0f + th) + 0.5f * x * (1.0f - th * th) * ds;
+  const float x2 = x * x;
+  const float s = kSqrt2OverPi * fmaf(kGeluCubic * x, x2, x);
+  const float ds = kSqrt2OverPi * fmaf(3.0f * kGeluCubic, x2, 1.0f);
+  const float e = __expf(fminf(-2.0f * s, 80.0f));
+  const float r = rcp_approx(1.0f + e);
+  return fmaf(2.0f * x * ds, (e * r) * r, r);
 }
 
 __device__ __forceinline__ uint64_t splitmix64_at(uint64_t seed, uint64_t e) {

@@ -1,6 +1,7 @@
 // HBM-bound kernels of the MLP block that do not fuse into a GEMM epilogue:
-//   * dropout backward + bias gradient:  dZ = dO * m / (1-p) (bf16),  db += sum_tok dZ
-//   * column sums:                        da_i += sum_tok dU_i
+//   * dropout backward + bias gradient:  dZ = dO * m / (1-p) (bf16),  db (+)= sum_tok dZ
+//   * column sums:                        da_i (+)= sum_tok dU_i
+//   (+)= adds to the accumulator, or overwrites it for the first micro-batch of a step
 //   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
 //
 // Column sums are deterministic: one CTA owns 64 columns for every row, each of
@@ -18,10 +19,10 @@ namespace gbmlp {
 constexpr int kColThreads = 256;  // 8 column groups (8 bf16 = 16 B each) x 32 row lanes
 constexpr int kColsPerCta = 64;
 
-// dZ = dO * keep * scale (rounded to bf16); db[c] += sum over rows of the rounded dZ.
+// dZ = dO * keep * scale (rounded to bf16); db[c] (+)= sum over rows of the rounded dZ.
 __global__ void __launch_bounds__(kColThreads)
     k_dropout_bwd_colsum(const uint16_t* __restrict__ dO, uint16_t* __restrict__ dZ, float* __restrict__ db,
-                         int64_t rows, int cols, DropoutParams drop) {
+                         int64_t rows, int cols, DropoutParams drop, int accumulate) {
   __shared__ float part[32][kColsPerCta + 1];
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
@@ -55,14 +56,15 @@ __global__ void __launch_bounds__(kColThreads)
     if (c < cols) {
       float tot = 0.0f;
       for (int k = 0; k < 32; ++k) tot += part[k][threadIdx.x];
-      db[c] += tot;
+      db[c] = accumulate ? db[c] + tot : tot;
     }
   }
 }
 
-// out[c] += sum over rows of x[r * ld + c], c < cols.
+// out[c] (+)= sum over rows of x[r * ld + c], c < cols.
 __global__ void __launch_bounds__(kColThreads)
-    k_colsum_bf16(const uint16_t* __restrict__ x, int64_t ld, float* __restrict__ out, int64_t rows, int cols) {
+    k_colsum_bf16(const uint16_t* __restrict__ x, int64_t ld, float* __restrict__ out, int64_t rows, int cols,
+                  int accumulate) {
   __shared__ float part[32][kColsPerCta + 1];
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
@@ -85,7 +87,7 @@ __global__ void __launch_bounds__(kColThreads)
     if (c < cols) {
       float tot = 0.0f;
       for (int k = 0; k < 32; ++k) tot += part[k][threadIdx.x];
-      out[c] += tot;
+      out[c] = accumulate ? out[c] + tot : tot;
     }
   }
 }

@@ -3,11 +3,13 @@
 //
 // Forward (per slice i, in turn):  F1  U_i, Y_i = GeLU(X A_i + a_i)        GEMM + GeLU epilogue
 //                                  F2  Z += Y_i B_i; last slice: O = R + dropout(Z + b)
-// Backward:                        B1  dZ = dropout'(dO), db += sum dZ       element-wise + column sum
+// Backward:                        B1  dZ = dropout'(dO), db (+)= sum dZ     element-wise + column sum
 //                   (per slice)    B2  dU_i = (dZ B_i^T) * GeLU'(U_i)      GEMM + GeLU' epilogue
-//                                      da_i += sum dU_i                    column sum
-//                                  B3  dB_i += Y_i^T dZ                    GEMM + fp32 accumulate
-//                                  B4  dA_i += X^T dU_i                    GEMM + fp32 accumulate
+//                                      da_i (+)= sum dU_i                  column sum
+//                                  B3  dB_i (+)= Y_i^T dZ                  GEMM + fp32 store / reduce-add
+//                                  B4  dA_i (+)= X^T dU_i                  GEMM + fp32 store / reduce-add
+// Weight and bias gradients are added to the fp32 accumulators, or, for the first
+// micro-batch of a step (accumulate = 0), stored into them.
 //                                  B5  dX (+)= dU_i A_i^T; last slice adds dO and writes bf16
 // The forward sum over slices (operator g of the Megatron MLP) and the backward sum
 // (operator f) are fp32 reductions in HBM on this GPU (STRONGHOLD slides, item 8).
@@ -174,6 +176,22 @@ int make_out_map(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, 
   return MLP_OK;
 }
 
+// 2-D bf16 tensor map of a GEMM output for TMA stores: box of 32 columns x 32
+// rows, 64-byte swizzle.
+int make_out_map_bf16(CUtensorMap* m, const uint16_t* base, int64_t cols, int64_t rows, int64_t ld) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled (bf16 output) failed (%d): cols %lld rows %lld ld %lld", (int)r,
+                (long long)cols, (long long)rows, (long long)ld);
+  return MLP_OK;
+}
+
 // Tensor map of one GEMM operand with `mn` rows/columns along M (or N) and `k`
 // along the reduction.  K-major: k contiguous; MN-major: m (or n) contiguous.
 int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int64_t k, int64_t ld,
@@ -183,8 +201,9 @@ int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int
 }
 
 template <bool AM, bool BM, bool PAIR>
-int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC, int M, int N,
-                  int K, const EpiParams& ep, int raster_n_fast, cudaStream_t stream, int trace_kind) {
+int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
+                  const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
+                  int raster_n_fast, cudaStream_t stream, int trace_kind) {
   using Cfg = GemmCfg<PAIR>;
   auto kern = k_gemm_bf16_tc<AM, BM, PAIR>;
   const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0);
@@ -231,10 +250,11 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, M, N, K, ep, raster_n_fast, st->status);
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, st->status);
   } else {
     const int grid = (int)(tiles < st->sms ? tiles : st->sms);
-    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, M, N, K, ep, raster_n_fast, st->status);
+    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                          st->status);
     e = cudaGetLastError();
   }
   trace_post(ts, stream, trace_kind, M, N, K);
@@ -249,28 +269,42 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
          int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
   const int mode = g_pair_mode.load(std::memory_order_relaxed);
   const bool pair = mode == 1 || (mode < 0 && M > kBM);
-  CUtensorMap mA, mB, mC;
+  CUtensorMap mA, mB, mC, mO0, mO1;
   int rc = operand_map(&mA, a, a_mn, M, K, lda, kBM);
   if (rc) return rc;
   rc = operand_map(&mB, b, b_mn, N, K, ldb, pair ? GemmCfg<true>::kBLoadN : GemmCfg<false>::kBLoadN);
   if (rc) return rc;
+  memset(&mC, 0, sizeof(mC));
+  memset(&mO0, 0, sizeof(mO0));
+  memset(&mO1, 0, sizeof(mO1));
   if (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add) {
     rc = make_out_map(&mC, ep.g_out, N, M, ep.ld);
     if (rc) return rc;
   } else {
-    memset(&mC, 0, sizeof(mC));
+    rc = make_out_map_bf16(&mO0, ep.out0, N, M, ep.ld);
+    if (rc) return rc;
+    if (ep.kind == kEpiGelu) {
+      rc = make_out_map_bf16(&mO1, ep.out1, N, M, ep.ld);
+      if (rc) return rc;
+    }
   }
   // Visit tiles so that the operand re-read across the sweep is the smaller one.
   const int raster_n_fast = M > N ? 1 : 0;
   if (!a_mn && b_mn)
-    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind)
-                : launch_gemm_t<false, true, false>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind);
+    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
+                                                                trace_kind)
+                : launch_gemm_t<false, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
+                                                                trace_kind);
   if (!a_mn && !b_mn)
-    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind)
-                : launch_gemm_t<false, false, false>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind);
+    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
+                                                                trace_kind)
+                : launch_gemm_t<false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
+                                                                trace_kind);
   if (a_mn && b_mn)
-    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind)
-                : launch_gemm_t<true, true, false>(st, mA, mB, mC, M, N, K, ep, raster_n_fast, stream, trace_kind);
+    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
+                                                                trace_kind)
+                : launch_gemm_t<true, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
+                                                                trace_kind);
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 
@@ -377,7 +411,7 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
 }
 
 int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t seed, uint64_t token_offset,
-            int residual_grad, const mlp_bf16* dO, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
+            int residual_grad, int accumulate, const mlp_bf16* dO, const mlp_bf16* X, const mlp_bf16* A, const mlp_bf16* B,
             const mlp_bf16* U, const mlp_bf16* Y, mlp_bf16* dZ, mlp_bf16* dU, float* dXacc, mlp_bf16* dX,
             float* dA, float* da, float* dB, float* db, void* stream) {
   int rc = check_shape(h, ffn, t, slice, tokens, p);
@@ -403,7 +437,8 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   if (first_call) {
     // B1: dZ = dO * m / (1 - p), db += sum_tok dZ
     const int ts = trace_pre(s);
-    k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dO, dZ, db, tokens, h, drop);
+    k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dO, dZ, db, tokens, h, drop,
+                                                                                      accumulate ? 1 : 0);
     trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
     rc = launch_check("dropout backward");
     if (rc) return rc;
@@ -422,20 +457,21 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     if (rc) return rc;
     // da_i += sum_tok dU_i
     const int ts = trace_pre(s);
-    k_colsum_bf16<<<(f + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dU + c, ffn, da + c, tokens, f);
+    k_colsum_bf16<<<(f + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dU + c, ffn, da + c, tokens, f,
+                                                                               accumulate ? 1 : 0);
     trace_post(ts, s, kTraceColsum, tokens, f, 0);
     rc = launch_check("bias-gradient column sum");
     if (rc) return rc;
-    // B3: dB_i += Y_i^T dZ                               (M = f, N = h, K = T)
+    // B3: dB_i (+)= Y_i^T dZ                             (M = f, N = h, K = T)
     EpiParams e3{};
-    e3.kind = kEpiF32Add;
+    e3.kind = accumulate ? kEpiF32Add : kEpiF32Store;
     e3.ld = h;
     e3.g_out = dB + c * h;
     rc = gemm(st, Y + c, true, ffn, dZ, true, h, f, h, T, e3, s, kTraceB3);
     if (rc) return rc;
-    // B4: dA_i += X^T dU_i                               (M = h, N = f, K = T)
+    // B4: dA_i (+)= X^T dU_i                             (M = h, N = f, K = T)
     EpiParams e4{};
-    e4.kind = kEpiF32Add;
+    e4.kind = accumulate ? kEpiF32Add : kEpiF32Store;
     e4.ld = ffn;
     e4.g_out = dA + c;
     rc = gemm(st, X, true, h, dU + c, true, ffn, h, f, T, e4, s, kTraceB4);

@@ -40,9 +40,13 @@ constexpr int kGemmThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kChunkBytes = 64 * kBK * 2;  // one 64 x BK box of an MN-major operand
 constexpr uint32_t kTmemCols = 2 * kBN;         // double-buffered accumulator
-// fp32 outputs leave through TMA: each epilogue warp stages 32 rows x 32 columns
-// (4 KB, 128-byte swizzled) in one of two buffers and issues a bulk store/reduce.
+// Outputs leave through TMA: each epilogue warp stages 32 rows x 32 columns in
+// one of two buffers and issues a bulk store (or, for fp32, a bulk reduce-add).
+// fp32 boxes are 4 KB with a 128-byte swizzle.
+// bf16 outputs likewise, as 32 x 32 boxes with a 64-byte swizzle (two outputs
+// per buffer for the GeLU epilogue, which writes U and Y).
 constexpr uint32_t kOutBoxBytes = 32 * 32 * 4;
+constexpr uint32_t kOutBoxBf16Bytes = 32 * 32 * 2;
 constexpr uint32_t kOutStageBytes = 4 * 2 * kOutBoxBytes;  // 4 warps x 2 buffers
 
 template <bool PAIR>
@@ -77,15 +81,6 @@ struct EpiParams {
   DropoutParams drop;
 };
 
-__device__ __forceinline__ void st_bf16x8(uint16_t* p, const float (&v)[8]) {
-  uint4 q;
-  q.x = pack_bf16x2(v[0], v[1]);
-  q.y = pack_bf16x2(v[2], v[3]);
-  q.z = pack_bf16x2(v[4], v[5]);
-  q.w = pack_bf16x2(v[6], v[7]);
-  *reinterpret_cast<uint4*>(p) = q;
-}
-
 __device__ __forceinline__ void ld_bf16x8(const uint16_t* p, float (&v)[8]) {
   const uint4 q = *reinterpret_cast<const uint4*>(p);
   v[0] = bf16lo(q.x); v[1] = bf16hi(q.x);
@@ -101,90 +96,86 @@ __device__ __forceinline__ void ld_f32x8(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
-__device__ __forceinline__ void st_f32x8(float* p, const float (&v)[8]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-
-// One thread, one row, 32 accumulator columns [col0, col0 + 32).  N % 8 == 0.
+// One thread, one row, 32 accumulator columns [col0, col0 + 32); N % 8 == 0.
+// Computes the bf16 output(s) of the fused epilogue, packed two per word:
+// o0 = U / O / dU / dX, o1 = Y (GeLU only).  Inputs are read only inside the
+// tensor (row < M, col < N); out-of-range lanes produce values the TMA store clips.
 template <int KIND>
-__device__ __forceinline__ void epilogue_chunk(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
-                                               int N) {
+__device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
+                                                int M, int N, uint32_t (&o0)[16], uint32_t (&o1)[16]) {
+  const bool row_ok = row < M;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const int col = col0 + 8 * g;
-    if (col >= N) break;
+    const bool col_ok = col < N;
+    const bool ok = row_ok && col_ok;
     float v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = __uint_as_float(r[8 * g + j]);
     const int64_t off = row * ep.ld + col;
     if constexpr (KIND == kEpiGelu) {
-      float bb[8], y[8];
-      ld_bf16x8(ep.bias + col, bb);
+      float bb[8] = {0, 0, 0, 0, 0, 0, 0, 0}, y[8];
+      if (col_ok) ld_bf16x8(ep.bias + col, bb);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         v[j] += bb[j];
         y[j] = gelu_f(v[j]);
       }
-      st_bf16x8(ep.out0 + off, v);
-      st_bf16x8(ep.out1 + off, y);
-    } else if constexpr (KIND == kEpiF32Store) {
-      st_f32x8(ep.g_out + off, v);
-    } else if constexpr (KIND == kEpiF32Add) {
-      float o[8];
-      ld_f32x8(ep.g_out + off, o);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) o[j] += v[j];
-      st_f32x8(ep.g_out + off, o);
+      for (int j = 0; j < 4; ++j) {
+        o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        o1[4 * g + j] = pack_bf16x2(y[2 * j], y[2 * j + 1]);
+      }
     } else if constexpr (KIND == kEpiDropRes) {
-      float bb[8], res[8];
-      if (ep.g_in != nullptr) {
+      float bb[8] = {0, 0, 0, 0, 0, 0, 0, 0}, res[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (ok && ep.g_in != nullptr) {
         float z[8];
         ld_f32x8(ep.g_in + off, z);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = z[j] + v[j];
       }
-      ld_bf16x8(ep.bias + col, bb);
-      ld_bf16x8(ep.in0 + off, res);
+      if (col_ok) ld_bf16x8(ep.bias + col, bb);
+      if (ok) ld_bf16x8(ep.in0 + off, res);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const bool keep = dropout_keep(ep.drop, row, col + j);
         v[j] = res[j] + (keep ? (v[j] + bb[j]) * ep.drop.scale : 0.0f);
       }
-      st_bf16x8(ep.out0 + off, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     } else if constexpr (KIND == kEpiDGelu) {
-      float u[8];
-      ld_bf16x8(ep.in0 + off, u);
+      float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (ok) ld_bf16x8(ep.in0 + off, u);
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] *= gelu_prime_f(u[j]);
-      st_bf16x8(ep.out0 + off, v);
-    } else if constexpr (KIND == kEpiResAdd) {
-      if (ep.g_in != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    } else {  // kEpiResAdd
+      if (ok && ep.g_in != nullptr) {
         float z[8];
         ld_f32x8(ep.g_in + off, z);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = z[j] + v[j];
       }
-      if (ep.in0 != nullptr) {
+      if (ok && ep.in0 != nullptr) {
         float res[8];
         ld_bf16x8(ep.in0 + off, res);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] += res[j];
       }
-      st_bf16x8(ep.out0 + off, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     }
   }
 }
 
 __device__ __forceinline__ void epilogue_dispatch(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
-                                                  int N) {
+                                                  int M, int N, uint32_t (&o0)[16], uint32_t (&o1)[16]) {
   switch (ep.kind) {
-    case kEpiGelu: epilogue_chunk<kEpiGelu>(ep, row, col0, r, N); break;
-    case kEpiF32Store: epilogue_chunk<kEpiF32Store>(ep, row, col0, r, N); break;
-    case kEpiF32Add: epilogue_chunk<kEpiF32Add>(ep, row, col0, r, N); break;
-    case kEpiDropRes: epilogue_chunk<kEpiDropRes>(ep, row, col0, r, N); break;
-    case kEpiDGelu: epilogue_chunk<kEpiDGelu>(ep, row, col0, r, N); break;
-    default: epilogue_chunk<kEpiResAdd>(ep, row, col0, r, N); break;
+    case kEpiGelu: epilogue_values<kEpiGelu>(ep, row, col0, r, M, N, o0, o1); break;
+    case kEpiDropRes: epilogue_values<kEpiDropRes>(ep, row, col0, r, M, N, o0, o1); break;
+    case kEpiDGelu: epilogue_values<kEpiDGelu>(ep, row, col0, r, M, N, o0, o1); break;
+    default: epilogue_values<kEpiResAdd>(ep, row, col0, r, M, N, o0, o1); break;
   }
 }
 
@@ -197,12 +188,14 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // A_MN / B_MN: operand stored MN-major (true) or K-major (false).
 // PAIR: launched as clusters of two CTAs (see the file comment).
 // tmC: fp32 output map (box 32 x 32, 128-byte swizzle) used by kEpiF32Store / kEpiF32Add.
+// tmO0 / tmO1: bf16 output maps (box 32 x 32, 64-byte swizzle) of out0 / out1.
 // raster_n_fast: tiles are visited with N varying fastest (else M fastest), so that
 // the operand re-read across the sweep is the smaller one and stays in L2.
 template <bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, int M, int N, int K, EpiParams ep, int raster_n_fast,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
+                   const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
                    int* status) {
   using Cfg = GemmCfg<PAIR>;
   constexpr int kStages = Cfg::kStages;
@@ -248,7 +241,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    if (tma_out) tma_prefetch_desc(&tmC);
+    if (tma_out) {
+      tma_prefetch_desc(&tmC);
+    } else {
+      tma_prefetch_desc(&tmO0);
+      if (ep.kind == kEpiGelu) tma_prefetch_desc(&tmO1);
+    }
   }
   if (warp == 1) {
     tmem_alloc<PAIR>(tmem_slot, kTmemCols);
@@ -468,8 +466,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             ++n_out;
           }
-        } else if (row < M && n0 + c0 < N) {
-          epilogue_dispatch(ep, row, n0 + c0, r, N);
+        } else if (n0 + c0 < N && m0 + quarter * 32 < M) {
+          // Warp-uniform, as above: bf16 output box(es) of 32 rows x 32 columns.
+          uint32_t o0[16], o1[16];
+          epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1);
+          uint8_t* box0 = my_out + (n_out & 1) * (2 * kOutBoxBf16Bytes);
+          uint8_t* box1 = box0 + kOutBoxBf16Bytes;
+          const bool two = ep.kind == kEpiGelu;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t off = lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4);
+            *reinterpret_cast<uint4*>(box0 + off) = make_uint4(o0[4 * j], o0[4 * j + 1], o0[4 * j + 2], o0[4 * j + 3]);
+            if (two)
+              *reinterpret_cast<uint4*>(box1 + off) =
+                  make_uint4(o1[4 * j], o1[4 * j + 1], o1[4 * j + 2], o1[4 * j + 3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmO0, box0, n0 + c0, m0 + quarter * 32);
+            if (two) tma_store_2d(&tmO1, box1, n0 + c0, m0 + quarter * 32);
+            bulk_commit();
+          }
+          ++n_out;
         }
       }
       tc_fence_before();

@@ -31,7 +31,7 @@ _f32 = ctypes.c_float
 
 _SIGNATURES = {
     "mlp_fwd": (_i32, [_i32, _i32, _i32, _i32, _i64, _f32, _u64, _u64] + [_vp] * 6 + [_vp, _vp, _vp, _vp, _vp]),
-    "mlp_bwd": (_i32, [_i32, _i32, _i32, _i32, _i64, _f32, _u64, _u64, _i32] + [_vp] * 6 + [_vp] * 4
+    "mlp_bwd": (_i32, [_i32, _i32, _i32, _i32, _i64, _f32, _u64, _u64, _i32, _i32] + [_vp] * 6 + [_vp] * 4
                 + [_vp] * 4 + [_vp]),
     "grad_accum_reset": (_i32, [_i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "mlp_sync_status": (_i32, [_vp]),
@@ -103,9 +103,10 @@ def mlp_fwd(h, ffn, t, slice_, tokens, p, seed, token_offset, X, A, a, B, b, R, 
                           _ptr(b), _ptr(R), _ptr(U), _ptr(Y), _ptr(Zacc), _ptr(O), _stream(stream)))
 
 
-def mlp_bwd(h, ffn, t, slice_, tokens, p, seed, token_offset, residual_grad, dO, X, A, B, U, Y, dZ, dU, dXacc, dX,
-            dA, da, dB, db, stream=None):
-    _check(load().mlp_bwd(h, ffn, t, slice_, tokens, p, seed, token_offset, int(residual_grad), _ptr(dO), _ptr(X),
+def mlp_bwd(h, ffn, t, slice_, tokens, p, seed, token_offset, residual_grad, accumulate, dO, X, A, B, U, Y, dZ, dU,
+            dXacc, dX, dA, da, dB, db, stream=None):
+    _check(load().mlp_bwd(h, ffn, t, slice_, tokens, p, seed, token_offset, int(residual_grad), int(accumulate),
+                          _ptr(dO), _ptr(X),
                           _ptr(A), _ptr(B), _ptr(U), _ptr(Y), _ptr(dZ), _ptr(dU), _ptr(dXacc), _ptr(dX), _ptr(dA),
                           _ptr(da), _ptr(dB), _ptr(db), _stream(stream)))
 
@@ -224,10 +225,13 @@ class BlockBuffers:
         self.db = torch.zeros(h, **f32)
 
 
-def block_step(wl, weights, X, dO, buf: BlockBuffers, token_offset=0, slice_mode="all", stream=None):
-    """One micro-batch forward + backward of workload ``wl`` (gradients accumulate).
+def block_step(wl, weights, X, dO, buf: BlockBuffers, token_offset=0, slice_mode="all", stream=None,
+               accumulate=True):
+    """One micro-batch forward + backward of workload ``wl``.
 
     slice_mode "all": one call each with slice = -1; "each": t calls per pass, in order.
+    accumulate: add this micro-batch's weight/bias gradients to buf's accumulators
+    (True) or overwrite them (False: the first micro-batch of a step).
     """
     A, a, B, b = weights
     T = X.shape[0]
@@ -236,5 +240,5 @@ def block_step(wl, weights, X, dO, buf: BlockBuffers, token_offset=0, slice_mode
         mlp_fwd(wl.h, wl.ffn, wl.t, i, T, wl.p, wl.seed, token_offset, X, A, a, B, b, None, buf.U, buf.Y, buf.Zacc,
                 buf.O, stream)
     for i in slices:
-        mlp_bwd(wl.h, wl.ffn, wl.t, i, T, wl.p, wl.seed, token_offset, 1, dO, X, A, B, buf.U, buf.Y, buf.dZ, buf.dU,
-                buf.dXacc, buf.dX, buf.dA, buf.da, buf.dB, buf.db, stream)
+        mlp_bwd(wl.h, wl.ffn, wl.t, i, T, wl.p, wl.seed, token_offset, 1, accumulate, dO, X, A, B, buf.U, buf.Y,
+                buf.dZ, buf.dU, buf.dXacc, buf.dX, buf.dA, buf.da, buf.dB, buf.db, stream)
