@@ -95,6 +95,12 @@ struct DeviceState {
   int max_pairs[8] = {};    // per CTA-pair instantiation: co-resident clusters of two
 };
 
+// L2 policies of the GEMMs' TMA copies (see k_gemm_bf16_tc): none by default.
+std::atomic<int> g_l2_hints{0};
+
+// Bytes of the smaller GEMM operand meant to stay in L2 during a grouped sweep.
+constexpr int64_t kGroupBytes = 32ll << 20;
+
 // -1: CTA pairs whenever a tile has more than 128 rows; 0: single CTAs; 1: CTA pairs.
 std::atomic<int> g_pair_mode{-1};
 
@@ -203,7 +209,7 @@ int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int
 template <bool AM, bool BM, bool PAIR>
 int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                   const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
-                  int raster_n_fast, cudaStream_t stream, int trace_kind) {
+                  int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind) {
   using Cfg = GemmCfg<PAIR>;
   auto kern = k_gemm_bf16_tc<AM, BM, PAIR>;
   const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0);
@@ -250,11 +256,12 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, st->status);
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group, l2_hints,
+                           st->status);
   } else {
     const int grid = (int)(tiles < st->sms ? tiles : st->sms);
     kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                          st->status);
+                                                          group, l2_hints, st->status);
     e = cudaGetLastError();
   }
   trace_post(ts, stream, trace_kind, M, N, K);
@@ -289,22 +296,36 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
     }
   }
   // Visit tiles so that the operand re-read across the sweep is the smaller one.
+  // When the two operands are of similar size (the weight-gradient GEMMs, whose
+  // reduction runs over the tokens), sweep the fast dimension in groups whose
+  // stripes of the smaller operand fit in L2 together (kGroupBytes); the larger
+  // operand is then read ceil(blocks / group) times instead of the smaller one
+  // being re-read from HBM for every wave.
   const int raster_n_fast = M > N ? 1 : 0;
+  const int64_t small_rows = M < N ? M : N;
+  const int64_t big_rows = M < N ? N : M;
+  int group = 0;
+  if (big_rows <= 8 * small_rows) {
+    const int64_t stripe_bytes = (int64_t)K * kBN * 2;  // one 256-row block of an operand
+    group = (int)(kGroupBytes / stripe_bytes);
+    if (group < 1) group = 1;
+  }
+  const int l2_hints = g_l2_hints.load(std::memory_order_relaxed);
   if (!a_mn && b_mn)
-    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
-                                                                trace_kind)
-                : launch_gemm_t<false, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
-                                                                trace_kind);
+    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                                group, l2_hints, stream, trace_kind)
+                : launch_gemm_t<false, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                                group, l2_hints, stream, trace_kind);
   if (!a_mn && !b_mn)
-    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
-                                                                trace_kind)
-                : launch_gemm_t<false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
-                                                                trace_kind);
+    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                                group, l2_hints, stream, trace_kind)
+                : launch_gemm_t<false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                                group, l2_hints, stream, trace_kind);
   if (a_mn && b_mn)
-    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
-                                                                trace_kind)
-                : launch_gemm_t<true, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, stream,
-                                                                trace_kind);
+    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                                group, l2_hints, stream, trace_kind)
+                : launch_gemm_t<true, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
+                                                                group, l2_hints, stream, trace_kind);
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 

@@ -191,12 +191,18 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // tmO0 / tmO1: bf16 output maps (box 32 x 32, 64-byte swizzle) of out0 / out1.
 // raster_n_fast: tiles are visited with N varying fastest (else M fastest), so that
 // the operand re-read across the sweep is the smaller one and stays in L2.
+// group: if > 0, the fast dimension is swept in groups of `group` blocks: all
+// tiles of those blocks (across the whole slow dimension) come before the next
+// group, so that only `group` stripes of the smaller operand need to stay in L2
+// while the larger operand streams past them.
+// l2_hints: L2 policy of the A loads (bits 0-1), the B loads (bits 2-3) and the
+// output stores (bits 4-5), an L2Hint each (kL2None: no hint).
 template <bool A_MN, bool B_MN, bool PAIR>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
-                   int* status) {
+                   int group, int l2_hints, int* status) {
   using Cfg = GemmCfg<PAIR>;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -214,8 +220,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = PAIR ? cluster_ctarank() : 0u;     // 0 = the CTA that issues the MMAs
-  const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
-  const int num_groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;   // CTA pair or single CTA
+  const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int num_m = (M + Cfg::kTileM - 1) / Cfg::kTileM;
   const int num_n = (N + kBN - 1) / kBN;
   const int num_tiles = num_m * num_n;
@@ -270,14 +276,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int tile_end = skip ? 0 : num_tiles;
 
   auto tile_origin = [&](int tile, int& m0, int& n0) {
-    int mb, nb;
-    if (raster_n_fast) {
-      nb = tile % num_n;
-      mb = tile / num_n;
-    } else {
-      mb = tile % num_m;
-      nb = tile / num_m;
-    }
+    // fast: blocks along the fast dimension; slow: along the other one
+    const int n_fast = raster_n_fast ? num_n : num_m;
+    const int n_slow = raster_n_fast ? num_m : num_n;
+    const int g = group > 0 ? group : n_fast;
+    const int gi = tile / (g * n_slow);             // group index
+    const int gw = min(g, n_fast - gi * g);         // width of this group
+    const int r = tile - gi * g * n_slow;
+    const int fast = gi * g + r % gw;
+    const int slow = r / gw;
+    const int mb = raster_n_fast ? slow : fast;
+    const int nb = raster_n_fast ? fast : slow;
     m0 = mb * Cfg::kTileM + (int)rank * kBM;  // this CTA's first row
     n0 = nb * kBN;
   };
@@ -285,13 +294,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      const int ha = l2_hints & 3, hb = (l2_hints >> 2) & 3;
+      const uint64_t pol_a = l2_policy(ha);
+      const uint64_t pol_b = l2_policy(hb);
       uint32_t issued[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) issued[s] = 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = group; tile < tile_end && ok; tile += num_groups) {
+      for (int tile = unit; tile < tile_end && ok; tile += num_units) {
         int m0, n0;
         tile_origin(tile, m0, n0);
         const int b_n0 = n0 + (PAIR ? (int)rank * Cfg::kBLoadN : 0);
@@ -310,32 +322,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
             if constexpr (A_MN) {
 #pragma unroll
-              for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(a_dst + j * kChunkBytes, &tmA, bar, m0 + 64 * j, k0);
+              for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(a_dst + j * kChunkBytes, &tmA, bar, m0 + 64 * j, k0, pol_a, ha != kL2None);
             } else {
-              tma_load_2d_pair(a_dst, &tmA, bar, k0, m0);
+              tma_load_2d_pair(a_dst, &tmA, bar, k0, m0, pol_a, ha != kL2None);
             }
             if constexpr (B_MN) {
 #pragma unroll
               for (int j = 0; j < Cfg::kBLoadN / 64; ++j)
-                tma_load_2d_pair(b_dst + j * kChunkBytes, &tmB, bar, b_n0 + 64 * j, k0);
+                tma_load_2d_pair(b_dst + j * kChunkBytes, &tmB, bar, b_n0 + 64 * j, k0, pol_b, hb != kL2None);
             } else {
-              tma_load_2d_pair(b_dst, &tmB, bar, k0, b_n0);
+              tma_load_2d_pair(b_dst, &tmB, bar, k0, b_n0, pol_b, hb != kL2None);
             }
           } else {
             mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
             if constexpr (A_MN) {
 #pragma unroll
               for (int j = 0; j < kBM / 64; ++j)
-                tma_load_2d(a_dst + j * kChunkBytes, &tmA, &full[stage], m0 + 64 * j, k0);
+                tma_load_2d(a_dst + j * kChunkBytes, &tmA, &full[stage], m0 + 64 * j, k0, pol_a, ha != kL2None);
             } else {
-              tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+              tma_load_2d(a_dst, &tmA, &full[stage], k0, m0, pol_a, ha != kL2None);
             }
             if constexpr (B_MN) {
 #pragma unroll
               for (int j = 0; j < Cfg::kBLoadN / 64; ++j)
-                tma_load_2d(b_dst + j * kChunkBytes, &tmB, &full[stage], b_n0 + 64 * j, k0);
+                tma_load_2d(b_dst + j * kChunkBytes, &tmB, &full[stage], b_n0 + 64 * j, k0, pol_b, hb != kL2None);
             } else {
-              tma_load_2d(b_dst, &tmB, &full[stage], k0, b_n0);
+              tma_load_2d(b_dst, &tmB, &full[stage], k0, b_n0, pol_b, hb != kL2None);
             }
           }
           ++issued[stage];
@@ -368,7 +380,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = group; tile < tile_end && ok; tile += num_groups) {
+      for (int tile = unit; tile < tile_end && ok; tile += num_units) {
         if (!(PAIR ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1) : mbar_wait(&acc_empty[acc], acc_phase ^ 1))) {
           record_status(status, kStatusTimeout, 3);
           break;
@@ -426,9 +438,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int row_in_tile = quarter * 32 + lane;
     uint8_t* my_out = sOut + (warp - 2) * 2 * kOutBoxBytes;
     uint32_t n_out = 0;  // boxes this warp has issued
+    const int hout = (l2_hints >> 4) & 3;
+    const uint64_t pol_out = l2_policy(hout);
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = group; tile < tile_end; tile += num_groups) {
+    for (int tile = unit; tile < tile_end; tile += num_units) {
       int m0, n0;
       tile_origin(tile, m0, n0);
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
@@ -459,9 +473,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             __syncwarp();
             if (lane == 0) {
               if (ep.kind == kEpiF32Add)
-                tma_reduce_add_2d(&tmC, box, n0 + c0, m0 + quarter * 32);
+                tma_reduce_add_2d(&tmC, box, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
               else
-                tma_store_2d(&tmC, box, n0 + c0, m0 + quarter * 32);
+                tma_store_2d(&tmC, box, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
               bulk_commit();
             }
             ++n_out;
@@ -486,8 +500,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmO0, box0, n0 + c0, m0 + quarter * 32);
-            if (two) tma_store_2d(&tmO1, box1, n0 + c0, m0 + quarter * 32);
+            tma_store_2d(&tmO0, box0, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+            if (two) tma_store_2d(&tmO1, box1, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
             bulk_commit();
           }
           ++n_out;
