@@ -40,6 +40,48 @@ def _peaks():
     return {"bf16_burst": 1900.0, "bf16_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
+# ----------------------------------------------------------------------------- ncu traffic
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_mtnlg_dram.md")
+GEMM_SOURCES = ["gemm_tc.cuh", "ptx.cuh", "block_math.cuh", "gb_mlp.cu"]
+
+
+def gemm_traffic_per_launch(workload: str):
+    """DRAM bytes (read + write) per GEMM launch from the committed ncu capture of
+    the MT-NLG layer, or None if the workload differs or the GEMM sources changed
+    since the capture (the file records a hash of them)."""
+    import hashlib
+    if workload != "mtnlg" or not os.path.exists(TRAFFIC_PROFILE):
+        return None
+    fields = {}
+    with open(TRAFFIC_PROFILE) as fh:
+        for line in fh:
+            if ":" in line and line.split(":")[0] in ("bytes_per_launch_avg", "source_sha256"):
+                k, v = line.split(":", 1)
+                fields[k] = v.strip()
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "transformer_lm_megatron_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("source_sha256") != h.hexdigest() or "bytes_per_launch_avg" not in fields:
+        return None
+    return float(fields["bytes_per_launch_avg"])
+
+
+def max_over_ranks(value: float, dist, device=None) -> float:
+    """The largest of every rank's value (the slowest rank's time); value itself on one rank."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica (weak scaling)."""
+    return world * flops_per_step * steps / (ms / 1e3) / 1e12
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
@@ -229,12 +271,9 @@ def run_ours(args, wl, rank, world, dist):
     ms = ev0.elapsed_time(ev1)
     if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
         raise RuntimeError(mlp.last_error())
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, dev)
     flops_step = wl.flops_total()
-    value = world * flops_step * args.steps / (ms / 1e3) / 1e12
+    value = job_throughput(flops_step, args.steps, world, ms)
 
     # ---- end to end through the public API: pinned host inputs in, results out.
     # Every micro-batch's X and dO are copied host->device and its O and dX
@@ -302,15 +341,11 @@ def run_ours(args, wl, rank, world, dist):
         e2e_run(args.steps, e0)
         e1.record(stream)
         torch.cuda.synchronize(dev)
-        ems = e0.elapsed_time(e1)
-        if dist is not None:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), dist, dev)
         # the last step's outputs reached the host intact
         ok = torch.equal(hO[wl.k - 1], bufs[(args.steps * wl.k - 1) % 2].O.cpu())
         act = wl.tokens * wl.h * 2 * wl.k
-        e2e = {"value": world * flops_step * args.steps / (ems / 1e3) / 1e12, "unit": UNIT,
+        e2e = {"value": job_throughput(flops_step, args.steps, world, ems), "unit": UNIT,
                "h2d_bytes_per_step": 2 * act, "d2h_bytes_per_step": 2 * act, "ms_per_step": ems / args.steps,
                "copies": "H2D/D2H on a second stream, double-buffered across micro-batches",
                "outputs_checked": bool(ok)}
@@ -321,6 +356,10 @@ def run_ours(args, wl, rank, world, dist):
     roofline = None
     if trace:
         roofline = trace.roofline(peaks, args.steps)
+        if roofline is not None:
+            roofline["traffic"] = gemm_traffic_per_launch(wl.name)
+            roofline["traffic_unit"] = "bytes per GEMM launch (DRAM read + write, ncu)"
+            roofline["algorithmic_bytes_per_launch"] = 2 * (wl.tokens * wl.h + wl.h * wl.ffn + wl.tokens * wl.ffn)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         w_host = tuple(x.cpu() for x in weights)
