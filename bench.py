@@ -42,7 +42,7 @@ def _peaks():
 
 # ----------------------------------------------------------------------------- ncu traffic
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_mtnlg_dram.md")
-GEMM_SOURCES = ["gemm_tc.cuh", "ptx.cuh", "block_math.cuh", "gb_mlp.cu"]
+GEMM_SOURCES = ["gemm_tc.cuh", "ptx.cuh", "block_math.cuh", "gemm_host.cuh"]
 
 
 def gemm_traffic_per_launch(workload: str):
@@ -180,6 +180,20 @@ def oracle_sample(wl, weights_host, n_tokens: int, slice_index: int = 0):
     orc.mlp_bwd(dO64, X64, A_i, B_i, fw["U"], fw["Y"], fw["keep"], 1, wl.p, mirror=True)
     dt = time.perf_counter() - t0
     return dt, 12 * n_tokens * wl.h * f
+
+
+def adam_oracle_sample(n=1 << 22):
+    """The Adam oracle (float64 numpy) on 4 Mi parameters, in the same unit as the GPU figure."""
+    import numpy as np
+    from oracle import adam_oracle as ado
+    rng = np.random.default_rng(0)
+    g, w = rng.standard_normal(n), rng.standard_normal(n) * 0.02
+    m, v = np.zeros(n), np.zeros(n)
+    t0 = time.perf_counter()
+    ado.adam_step(g, w, m, v, 1, 5e-5, 0.9, 0.95, 1e-8, 0.1)
+    dt = time.perf_counter() - t0
+    return {"value": 30 * n / dt / 1e9, "unit": "GB/s (30 B per parameter)", "cores": _cpu_cores(),
+            "kind": "oracle", "sample": f"{n} parameters, one step, float64 numpy, {dt * 1e3:.0f} ms"}
 
 
 def _cpu_cores():
@@ -373,6 +387,39 @@ def run_ours(args, wl, rank, world, dist):
                "copies": "H2D/D2H on a second stream, double-buffered across micro-batches",
                "outputs_checked": bool(ok)}
 
+    # ---- next row: the mixed-precision Adam step over the block's parameters,
+    # reading the fp32 gradients the step accumulated (30 bytes per parameter).
+    adam = None
+    if not args.no_adam:
+        masters = [w.float() for w in weights]
+        ms_state = [torch.zeros_like(x) for x in masters]
+        vs_state = [torch.zeros_like(x) for x in masters]
+        grads = [buf.dA, buf.da, buf.dB, buf.db]
+        hp = dict(lr=5e-5, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.1, grad_scale=1.0 / wl.k)
+
+        def adam_all(step):
+            for gr, w32, mm, vv, w16 in zip(grads, masters, ms_state, vs_state, weights):
+                mlp.adam_step(gr, w32, mm, vv, w16, step=step, stream=stream, **hp)
+
+        for s_ in range(1, 3):
+            adam_all(s_)
+        torch.cuda.synchronize(dev)
+        a_steps = 10
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for s_ in range(3, 3 + a_steps):
+            adam_all(s_)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        a_ms = a0.elapsed_time(a1) / a_steps
+        n_params = sum(x.numel() for x in masters)
+        a_bytes = 30 * n_params
+        adam = {"params": n_params, "ms_per_step": a_ms, "bytes_per_step": a_bytes,
+                "achieved_GBps": a_bytes / (a_ms / 1e3) / 1e9, "launches_per_step": 4,
+                "hyper": {k: v for k, v in hp.items()}}
+        del masters, ms_state, vs_state
+
     # ---- HBM-bound kernels: the reset pass (R0) is not part of a step when the
     # first micro-batch writes the gradients, so it is traced here on its own.
     reset_ms = None
@@ -403,6 +450,11 @@ def run_ours(args, wl, rank, world, dist):
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
                "sample": f"{args.cpu_tokens} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, "
                          f"float64 numpy, {dt:.1f} s"}
+    if adam is not None:
+        adam["peak_GBps"] = peaks["hbm_gbs"]
+        adam["frac"] = adam["achieved_GBps"] / peaks["hbm_gbs"]
+        if world == 1 and not args.no_cpu_baseline:
+            adam["cpu_baseline"] = adam_oracle_sample()
     burst = peaks["bf16_burst"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -423,6 +475,7 @@ def run_ours(args, wl, rank, world, dist):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clock_info,
+        "next_rows": {"adam_step": adam},
     }
     print(json.dumps(line), flush=True)
 
@@ -439,6 +492,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", dest="trace", action="store_false")
+    ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
     ap.add_argument("--reset-each-step", action="store_true",
                     help="time grad_accum_reset + all micro-batches adding, instead of the first writing")
     args = ap.parse_args()

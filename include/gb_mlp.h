@@ -130,6 +130,23 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
 int grad_accum_reset(int h, int ffn, float* dA, float* da, float* dB, float* db, void* stream);
 
 /*
+ * adam_step - one mixed-precision Adam update (decoupled weight decay) of n
+ * parameters from their fp32 gradient accumulator.  The pages give the cost of
+ * mixed-precision Adam, about 20 bytes of training state per parameter ("Using
+ * DeepSpeed and Megatron to Train Megatron-Turing NLG 530B", Key points); the
+ * update is the published algorithm (Kingma & Ba 2015; Loshchilov & Hutter 2019):
+ *   g = grad * grad_scale;  m = beta1 m + (1-beta1) g;  v = beta2 v + (1-beta2) g^2
+ *   master = master (1 - lr weight_decay) - lr/(1-beta1^step) m / (sqrt(v/(1-beta2^step)) + eps)
+ *   weight = bf16(master)   (round to nearest even)
+ * grad [n] fp32 (read only), master, m, v [n] fp32 (updated in place), weight [n]
+ * bf16 (written): device pointers; grad, master, m, v 16-byte aligned, weight
+ * 8-byte aligned.  step >= 1 counts updates; 0 <= beta1, beta2 < 1; eps > 0;
+ * lr, weight_decay >= 0.  Returns MLP_OK or an error code (nothing enqueued).
+ */
+int adam_step(int64_t n, const float* grad, float grad_scale, float* master, float* m, float* v, mlp_bf16* weight,
+              float lr, float beta1, float beta2, float eps, float weight_decay, int step, void* stream);
+
+/*
  * mlp_sync_status - synchronise `stream`, then return and clear the device status
  * word: MLP_OK, or MLP_ETIMEOUT if a kernel gave up on a bounded wait since the
  * last call (mlp_last_error() then names the wait), or MLP_ECUDA.
@@ -185,7 +202,8 @@ int mlp_trace_begin(int capacity);
  * mlp_trace_end - stop tracing, wait for the traced launches and report up to
  * max_entries of them in launch order: kinds[i] (0..5 = the GEMMs F1, F2, B2, B3,
  * B4, B5 of the forward/backward; 10 = dropout backward + db; 11 = column sum
- * for da; 12 = accumulator reset), mnk[3i..3i+2] = the launch's M, N, K (GEMMs)
+ * for da; 12 = accumulator reset; 14 = adam_step), mnk[3i..3i+2] = the launch's
+ * M, N, K (GEMMs)
  * or rows, columns, 0, and ms[i] = its device time in milliseconds.  Any output
  * pointer may be NULL.  Returns the number of entries written, or an error code.
  */

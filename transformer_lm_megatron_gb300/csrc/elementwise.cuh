@@ -5,7 +5,7 @@
 //   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
 //
 // Column sums are deterministic: one CTA owns 64 columns for every row, each of
-// its 32 row-lanes sums a fixed row subset, and the 32 partial sums are added in
+// its 64 row-lanes sums a fixed row subset, and the 64 partial sums are added in
 // a fixed order.  Loads and stores are 16-byte vectors; a warp covers four
 // 128-byte row segments per instruction.
 #pragma once
@@ -16,36 +16,53 @@
 
 namespace gbmlp {
 
-constexpr int kColThreads = 256;  // 8 column groups (8 bf16 = 16 B each) x 32 row lanes
+constexpr int kColRowLanes = 64;                 // threads along the rows of a column strip
+constexpr int kColThreads = 8 * kColRowLanes;    // 8 column groups (8 bf16 = 16 B each) x row lanes
 constexpr int kColsPerCta = 64;
 
+// Fixed-order sum of the row lanes' partial column sums; part is [kColRowLanes][kColsPerCta + 1].
+__device__ __forceinline__ float colsum_reduce(float (*part)[kColsPerCta + 1], int col_in_cta) {
+  float tot = 0.0f;
+  for (int k = 0; k < kColRowLanes; ++k) tot += part[k][col_in_cta];
+  return tot;
+}
+
 // dZ = dO * keep * scale (rounded to bf16); db[c] (+)= sum over rows of the rounded dZ.
+// Each thread handles two rows per iteration so that two 16-byte loads are in flight.
 __global__ void __launch_bounds__(kColThreads)
     k_dropout_bwd_colsum(const uint16_t* __restrict__ dO, uint16_t* __restrict__ dZ, float* __restrict__ db,
                          int64_t rows, int cols, DropoutParams drop, int accumulate) {
-  __shared__ float part[32][kColsPerCta + 1];
+  __shared__ float part[kColRowLanes][kColsPerCta + 1];
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
   const int col = blockIdx.x * kColsPerCta + cg * 8;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (col < cols) {
-    for (int64_t r = rl; r < rows; r += 32) {
-      const int64_t off = r * cols + col;
-      const uint4 q = *reinterpret_cast<const uint4*>(dO + off);
-      float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
-                    bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
+    for (int64_t r0 = rl; r0 < rows; r0 += 2 * kColRowLanes) {
+      const int64_t r1 = r0 + kColRowLanes;
+      const bool two = r1 < rows;
+      const uint4 q0 = *reinterpret_cast<const uint4*>(dO + r0 * cols + col);
+      const uint4 q1 = two ? *reinterpret_cast<const uint4*>(dO + r1 * cols + col) : make_uint4(0, 0, 0, 0);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool keep = dropout_keep(drop, r, col + j);
-        v[j] = round_bf16_f(keep ? v[j] * drop.scale : 0.0f);
-        s[j] += v[j];
+      for (int half = 0; half < 2; ++half) {
+        if (half == 1 && !two) break;
+        const uint4 q = half ? q1 : q0;
+        const int64_t r = half ? r1 : r0;
+        float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
+                      bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
+        const uint32_t keep = dropout_keep8(drop, r, col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[j] = round_bf16_f(((keep >> j) & 1u) ? v[j] * drop.scale : 0.0f);
+          s[j] += v[j];
+        }
+        uint4 o;
+        o.x = pack_bf16x2(v[0], v[1]);
+        o.y = pack_bf16x2(v[2], v[3]);
+        o.z = pack_bf16x2(v[4], v[5]);
+        o.w = pack_bf16x2(v[6], v[7]);
+        *reinterpret_cast<uint4*>(dZ + r * cols + col) = o;
       }
-      uint4 o;
-      o.x = pack_bf16x2(v[0], v[1]);
-      o.y = pack_bf16x2(v[2], v[3]);
-      o.z = pack_bf16x2(v[4], v[5]);
-      o.w = pack_bf16x2(v[6], v[7]);
-      *reinterpret_cast<uint4*>(dZ + off) = o;
     }
   }
 #pragma unroll
@@ -54,8 +71,7 @@ __global__ void __launch_bounds__(kColThreads)
   if (threadIdx.x < kColsPerCta) {
     const int c = blockIdx.x * kColsPerCta + threadIdx.x;
     if (c < cols) {
-      float tot = 0.0f;
-      for (int k = 0; k < 32; ++k) tot += part[k][threadIdx.x];
+      const float tot = colsum_reduce(part, threadIdx.x);
       db[c] = accumulate ? db[c] + tot : tot;
     }
   }
@@ -65,18 +81,24 @@ __global__ void __launch_bounds__(kColThreads)
 __global__ void __launch_bounds__(kColThreads)
     k_colsum_bf16(const uint16_t* __restrict__ x, int64_t ld, float* __restrict__ out, int64_t rows, int cols,
                   int accumulate) {
-  __shared__ float part[32][kColsPerCta + 1];
+  __shared__ float part[kColRowLanes][kColsPerCta + 1];
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
   const int col = blockIdx.x * kColsPerCta + cg * 8;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (col < cols) {
-    for (int64_t r = rl; r < rows; r += 32) {
-      const uint4 q = *reinterpret_cast<const uint4*>(x + r * ld + col);
-      s[0] += bf16lo(q.x); s[1] += bf16hi(q.x);
-      s[2] += bf16lo(q.y); s[3] += bf16hi(q.y);
-      s[4] += bf16lo(q.z); s[5] += bf16hi(q.z);
-      s[6] += bf16lo(q.w); s[7] += bf16hi(q.w);
+    for (int64_t r0 = rl; r0 < rows; r0 += 2 * kColRowLanes) {
+      const int64_t r1 = r0 + kColRowLanes;
+      const uint4 q0 = *reinterpret_cast<const uint4*>(x + r0 * ld + col);
+      const uint4 q1 = r1 < rows ? *reinterpret_cast<const uint4*>(x + r1 * ld + col) : make_uint4(0, 0, 0, 0);
+      s[0] += bf16lo(q0.x); s[1] += bf16hi(q0.x);
+      s[2] += bf16lo(q0.y); s[3] += bf16hi(q0.y);
+      s[4] += bf16lo(q0.z); s[5] += bf16hi(q0.z);
+      s[6] += bf16lo(q0.w); s[7] += bf16hi(q0.w);
+      s[0] += bf16lo(q1.x); s[1] += bf16hi(q1.x);
+      s[2] += bf16lo(q1.y); s[3] += bf16hi(q1.y);
+      s[4] += bf16lo(q1.z); s[5] += bf16hi(q1.z);
+      s[6] += bf16lo(q1.w); s[7] += bf16hi(q1.w);
     }
   }
 #pragma unroll
@@ -85,8 +107,7 @@ __global__ void __launch_bounds__(kColThreads)
   if (threadIdx.x < kColsPerCta) {
     const int c = blockIdx.x * kColsPerCta + threadIdx.x;
     if (c < cols) {
-      float tot = 0.0f;
-      for (int k = 0; k < 32; ++k) tot += part[k][threadIdx.x];
+      const float tot = colsum_reduce(part, threadIdx.x);
       out[c] = accumulate ? out[c] + tot : tot;
     }
   }
@@ -100,10 +121,22 @@ __global__ void k_zero_f32(float* __restrict__ p, int64_t n) {
     p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// m[r * cols + c] = keep(r, c) ? 1 : 0.
+// m[r * cols + c] = keep(r, c) ? 1 : 0, eight columns per thread with the same
+// routine the block's kernels use (cols % 8 == 0), else one element per thread.
 __global__ void k_dropout_mask(uint8_t* __restrict__ m, int64_t rows, int cols, DropoutParams drop) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  if (cols % 8 == 0) {
+    const int64_t n8 = rows * (int64_t)(cols / 8);
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += stride) {
+      const int64_t r = i / (cols / 8);
+      const int64_t c0 = (i - r * (cols / 8)) * 8;
+      const uint32_t bits = dropout_keep8(drop, r, c0);
+      for (int j = 0; j < 8; ++j) m[r * cols + c0 + j] = (bits >> j) & 1u;
+    }
+    return;
+  }
   const int64_t n = rows * (int64_t)cols;
-  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += stride) {
     const int64_t r = i / cols;
     const int64_t c = i - r * cols;
     m[i] = dropout_keep(drop, r, c) ? 1 : 0;

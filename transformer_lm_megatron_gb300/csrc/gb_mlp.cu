@@ -24,6 +24,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "adam.cuh"
 #include "elementwise.cuh"
 #include "gb_mlp.h"
 #include "gemm_tc.cuh"
@@ -56,7 +57,7 @@ TraceState g_trace;
 // Kernel identifiers reported by the trace.
 enum TraceKind {
   kTraceF1 = 0, kTraceF2 = 1, kTraceB2 = 2, kTraceB3 = 3, kTraceB4 = 4, kTraceB5 = 5,
-  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13
+  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13, kTraceAdam = 14
 };
 
 // Records the start event of the next launch; returns its slot or -1.
@@ -95,14 +96,6 @@ struct DeviceState {
   int max_pairs[8] = {};    // per CTA-pair instantiation: co-resident clusters of two
 };
 
-// L2 policies of the GEMMs' TMA copies (see k_gemm_bf16_tc): none by default.
-std::atomic<int> g_l2_hints{0};
-
-// Bytes of the smaller GEMM operand meant to stay in L2 during a grouped sweep.
-constexpr int64_t kGroupBytes = 32ll << 20;
-
-// -1: CTA pairs whenever a tile has more than 128 rows; 0: single CTAs; 1: CTA pairs.
-std::atomic<int> g_pair_mode{-1};
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
@@ -148,186 +141,7 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows, row
-// pitch `ld` elements; box {box_inner, box_outer}; 128-byte swizzle; out-of-range
-// elements read as zero.
-int make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
-             uint32_t box_outer) {
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled failed (%d): inner %lld outer %lld ld %lld", (int)r,
-                (long long)inner, (long long)outer, (long long)ld);
-  return MLP_OK;
-}
-
-// 2-D fp32 tensor map of a GEMM output for TMA stores / reduce-adds: box of 32
-// columns x 32 rows, 128-byte swizzle.
-int make_out_map(CUtensorMap* m, const float* base, int64_t cols, int64_t rows, int64_t ld) {
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled (fp32 output) failed (%d): cols %lld rows %lld ld %lld", (int)r,
-                (long long)cols, (long long)rows, (long long)ld);
-  return MLP_OK;
-}
-
-// 2-D bf16 tensor map of a GEMM output for TMA stores: box of 32 columns x 32
-// rows, 64-byte swizzle.
-int make_out_map_bf16(CUtensorMap* m, const uint16_t* base, int64_t cols, int64_t rows, int64_t ld) {
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {32, 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled (bf16 output) failed (%d): cols %lld rows %lld ld %lld", (int)r,
-                (long long)cols, (long long)rows, (long long)ld);
-  return MLP_OK;
-}
-
-// Tensor map of one GEMM operand with `mn` rows/columns along M (or N) and `k`
-// along the reduction.  K-major: k contiguous; MN-major: m (or n) contiguous.
-int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int64_t k, int64_t ld,
-                uint32_t tile_mn) {
-  if (mn_major) return make_map(m, base, mn, k, ld, 64, kBK);
-  return make_map(m, base, k, mn, ld, kBK, tile_mn);
-}
-
-template <bool AM, bool BM, bool PAIR>
-int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
-                  const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
-                  int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind) {
-  using Cfg = GemmCfg<PAIR>;
-  auto kern = k_gemm_bf16_tc<AM, BM, PAIR>;
-  const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0);
-  if (!st->gemm_attr[slot]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemBytes);
-    if (e != cudaSuccess) return fail(MLP_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    if (PAIR) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-      cudaLaunchConfig_t qc = {};
-      qc.gridDim = dim3(2 * (unsigned)st->sms, 1, 1);
-      qc.blockDim = dim3(kGemmThreads, 1, 1);
-      qc.dynamicSmemBytes = Cfg::kSmemBytes;
-      cudaLaunchAttribute qa[1];
-      qa[0].id = cudaLaunchAttributeClusterDimension;
-      qa[0].val.clusterDim.x = 2;
-      qa[0].val.clusterDim.y = 1;
-      qa[0].val.clusterDim.z = 1;
-      qc.attrs = qa;
-      qc.numAttrs = 1;
-      int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, kern, &qc);
-      if (e != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        n = st->sms / 2;
-      }
-      st->max_pairs[slot] = n;
-    }
-    st->gemm_attr[slot] = true;
-  }
-  const int64_t tiles = (int64_t)((M + Cfg::kTileM - 1) / Cfg::kTileM) * ((N + kBN - 1) / kBN);
-  const int ts = trace_pre(stream);
-  cudaError_t e;
-  if (PAIR) {
-    const int pairs = (int)(tiles < st->max_pairs[slot] ? tiles : st->max_pairs[slot]);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group, l2_hints,
-                           st->status);
-  } else {
-    const int grid = (int)(tiles < st->sms ? tiles : st->sms);
-    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                          group, l2_hints, st->status);
-    e = cudaGetLastError();
-  }
-  trace_post(ts, stream, trace_kind, M, N, K);
-  g_launches.fetch_add(1, std::memory_order_relaxed);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(MLP_ECUDA, "GEMM launch: %s", cudaGetErrorString(e));
-  return MLP_OK;
-}
-
-// D[M, N] = A(M x K) B(K x N) with the given operand layouts and epilogue.
-int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, bool b_mn, int64_t ldb, int M, int N,
-         int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
-  const int mode = g_pair_mode.load(std::memory_order_relaxed);
-  const bool pair = mode == 1 || (mode < 0 && M > kBM);
-  CUtensorMap mA, mB, mC, mO0, mO1;
-  int rc = operand_map(&mA, a, a_mn, M, K, lda, kBM);
-  if (rc) return rc;
-  rc = operand_map(&mB, b, b_mn, N, K, ldb, pair ? GemmCfg<true>::kBLoadN : GemmCfg<false>::kBLoadN);
-  if (rc) return rc;
-  memset(&mC, 0, sizeof(mC));
-  memset(&mO0, 0, sizeof(mO0));
-  memset(&mO1, 0, sizeof(mO1));
-  if (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add) {
-    rc = make_out_map(&mC, ep.g_out, N, M, ep.ld);
-    if (rc) return rc;
-  } else {
-    rc = make_out_map_bf16(&mO0, ep.out0, N, M, ep.ld);
-    if (rc) return rc;
-    if (ep.kind == kEpiGelu) {
-      rc = make_out_map_bf16(&mO1, ep.out1, N, M, ep.ld);
-      if (rc) return rc;
-    }
-  }
-  // Visit tiles so that the operand re-read across the sweep is the smaller one.
-  // When the two operands are of similar size (the weight-gradient GEMMs, whose
-  // reduction runs over the tokens), sweep the fast dimension in groups whose
-  // stripes of the smaller operand fit in L2 together (kGroupBytes); the larger
-  // operand is then read ceil(blocks / group) times instead of the smaller one
-  // being re-read from HBM for every wave.
-  const int raster_n_fast = M > N ? 1 : 0;
-  const int64_t small_rows = M < N ? M : N;
-  const int64_t big_rows = M < N ? N : M;
-  int group = 0;
-  if (big_rows <= 8 * small_rows) {
-    const int64_t stripe_bytes = (int64_t)K * kBN * 2;  // one 256-row block of an operand
-    group = (int)(kGroupBytes / stripe_bytes);
-    if (group < 1) group = 1;
-  }
-  const int l2_hints = g_l2_hints.load(std::memory_order_relaxed);
-  if (!a_mn && b_mn)
-    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind)
-                : launch_gemm_t<false, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind);
-  if (!a_mn && !b_mn)
-    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind)
-                : launch_gemm_t<false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind);
-  if (a_mn && b_mn)
-    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind)
-                : launch_gemm_t<true, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind);
-  return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
-}
+#include "gemm_host.cuh"
 
 DropoutParams make_dropout(float p, uint64_t seed, uint64_t token_offset, int h) {
   DropoutParams d;
@@ -538,6 +352,43 @@ int grad_accum_reset(int h, int ffn, float* dA, float* da, float* dB, float* db,
     if (rc) return rc;
   }
   return MLP_OK;
+}
+
+int adam_step(int64_t n, const float* grad, float grad_scale, float* master, float* m, float* v, mlp_bf16* weight,
+              float lr, float beta1, float beta2, float eps, float weight_decay, int step, void* stream) {
+  if (n <= 0) return fail(MLP_EINVAL, "adam_step: n = %lld must be positive", (long long)n);
+  if (step < 1) return fail(MLP_EINVAL, "adam_step: step = %d must be >= 1", step);
+  if (!(beta1 >= 0.0f && beta1 < 1.0f && beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(MLP_EINVAL, "adam_step: betas (%g, %g) not in [0, 1)", (double)beta1, (double)beta2);
+  if (!(eps > 0.0f) || !(lr >= 0.0f) || !(weight_decay >= 0.0f))
+    return fail(MLP_EINVAL, "adam_step: eps must be > 0, lr and weight_decay >= 0");
+  int rc = check_ptrs("adam_step", {grad, master, m, v});
+  if (rc) return rc;
+  if (weight == nullptr || (reinterpret_cast<uintptr_t>(weight) & 7u) != 0)
+    return fail(weight == nullptr ? MLP_EINVAL : MLP_EALIGN, "adam_step: weight NULL or not 8-byte aligned");
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  AdamParams p;
+  p.grad_scale = grad_scale;
+  p.beta1 = beta1;
+  p.one_minus_beta1 = 1.0f - beta1;
+  p.beta2 = beta2;
+  p.one_minus_beta2 = 1.0f - beta2;
+  const double bc1 = 1.0 - std::pow((double)beta1, step);
+  const double bc2 = 1.0 - std::pow((double)beta2, step);
+  p.step_size = (float)((double)lr / bc1);
+  p.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  p.eps = eps;
+  p.decay = (float)(1.0 - (double)lr * (double)weight_decay);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t blocks = (n / 4 + 255) / 256;
+  if (blocks > (int64_t)st->sms * 8) blocks = (int64_t)st->sms * 8;
+  if (blocks < 1) blocks = 1;
+  const int ts = trace_pre(s);
+  k_adam_step<<<(int)blocks, 256, 0, s>>>(n, grad, master, m, v, weight, p);
+  trace_post(ts, s, kTraceAdam, n, 0, 0);
+  return launch_check("adam_step");
 }
 
 int mlp_sync_status(void* stream) {

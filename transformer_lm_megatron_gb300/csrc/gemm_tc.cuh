@@ -136,11 +136,9 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row
       }
       if (col_ok) ld_bf16x8(ep.bias + col, bb);
       if (ok) ld_bf16x8(ep.in0 + off, res);
+      const uint32_t keep = dropout_keep8(ep.drop, row, col);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool keep = dropout_keep(ep.drop, row, col + j);
-        v[j] = res[j] + (keep ? (v[j] + bb[j]) * ep.drop.scale : 0.0f);
-      }
+      for (int j = 0; j < 8; ++j) v[j] = res[j] + (((keep >> j) & 1u) ? (v[j] + bb[j]) * ep.drop.scale : 0.0f);
 #pragma unroll
       for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     } else if constexpr (KIND == kEpiDGelu) {

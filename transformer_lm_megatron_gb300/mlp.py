@@ -41,6 +41,7 @@ _SIGNATURES = {
     "mlp_wait_timeout_probe": (_i32, [_u64, _vp]),
     "mlp_launch_count": (_u64, []),
     "mlp_set_cta_pair": (_i32, [_i32]),
+    "adam_step": (_i32, [_i64, _vp, _f32, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i32, _vp]),
     "mlp_fwd_static_scratch": (_i32, [_i32, _i32, _i32, _i32, _i64, _f32, _u64, _u64] + [_vp] * 6 + [_vp, _vp, _vp, _vp]),
     "mlp_trace_begin": (_i32, [_i32]),
     "mlp_trace_end": (_i32, [_i32, _vp, _vp, _vp]),
@@ -123,6 +124,17 @@ def grad_accum_reset(h, ffn, dA, da, dB, db, stream=None):
     _check(load().grad_accum_reset(h, ffn, _ptr(dA), _ptr(da), _ptr(dB), _ptr(db), _stream(stream)))
 
 
+def adam_step(grad, master, m, v, weight, lr, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0, step=1,
+              grad_scale=1.0, stream=None):
+    """One mixed-precision Adam update of a parameter tensor (see include/gb_mlp.h)."""
+    n = grad.numel()
+    for t in (master, m, v, weight):
+        if t.numel() != n:
+            raise ValueError("adam_step: all tensors need the same number of elements")
+    _check(load().adam_step(n, _ptr(grad), grad_scale, _ptr(master), _ptr(m), _ptr(v), _ptr(weight), lr, beta1,
+                            beta2, eps, weight_decay, step, _stream(stream)))
+
+
 def mlp_sync_status(stream=None) -> int:
     return load().mlp_sync_status(_stream(stream))
 
@@ -149,7 +161,7 @@ def mlp_set_cta_pair(mode: int):
 
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
                3: "B3 gemm Y_i^T.dZ (+= dB)", 4: "B4 gemm X^T.dU_i (+= dA)", 5: "B5 gemm dU_i.A_i^T (+dO)",
-               10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset"}
+               10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset", 14: "adam step"}
 GEMM_KINDS = (0, 1, 2, 3, 4, 5)
 
 
