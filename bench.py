@@ -157,29 +157,39 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- CPU oracle sample
-def oracle_sample(wl, weights_host, n_tokens: int, slice_index: int = 0):
-    """Times the oracle (float64, host cores) on a bounded sample of the workload:
-    ``n_tokens`` tokens through one slice (A_i columns, B_i rows) forward+backward.
-    Returns (seconds, algorithmic flops of the sample)."""
-    import numpy as np
+def oracle_sample_inputs(wl, weights_host, n_tokens: int, slice_index: int = 0):
+    """Float64 inputs of the CPU sample: ``n_tokens`` tokens and slice ``slice_index``
+    (A_i columns, B_i rows) of the workload's seeded weights."""
     from oracle import mlp_oracle as orc
     from transformer_lm_megatron_gb300 import inputs as gin
 
     A, a, B, b = weights_host
     f = wl.f
     cols = slice(slice_index * f, (slice_index + 1) * f)
-    A_i = orc.bf16_to_f64(gin.bf16_bits(A[:, cols]))
-    a_i = orc.bf16_to_f64(gin.bf16_bits(a[cols]))
-    B_i = orc.bf16_to_f64(gin.bf16_bits(B[cols, :]))
-    b64 = orc.bf16_to_f64(gin.bf16_bits(b))
     X, dO = gin.make_microbatch(n_tokens, wl.h, 0)
-    X64 = orc.bf16_to_f64(gin.bf16_bits(X))
-    dO64 = orc.bf16_to_f64(gin.bf16_bits(dO))
+    dec = lambda t: orc.bf16_to_f64(gin.bf16_bits(t))  # noqa: E731
+    return dec(X), dec(dO), dec(A[:, cols]), dec(a[cols]), dec(B[cols, :]), dec(b)
+
+
+def oracle_sample(wl, sample_inputs):
+    """Times the oracle (float64, host cores) forward+backward on a prepared sample.
+    Returns (seconds, algorithmic flops of the sample)."""
+    from oracle import mlp_oracle as orc
+    X64, dO64, A_i, a_i, B_i, b64 = sample_inputs
     t0 = time.perf_counter()
     fw = orc.mlp_fwd(X64, A_i, a_i, B_i, b64, 1, wl.p, wl.seed, mirror=True)
     orc.mlp_bwd(dO64, X64, A_i, B_i, fw["U"], fw["Y"], fw["keep"], 1, wl.p, mirror=True)
     dt = time.perf_counter() - t0
-    return dt, 12 * n_tokens * wl.h * f
+    return dt, 12 * X64.shape[0] * wl.h * A_i.shape[1]
+
+
+def workload_config(wl, slice_mode, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": wl.name, "tokens": wl.tokens, "h": wl.h, "ffn": wl.ffn, "t": wl.t,
+            "micro_batches": wl.k, "dropout": wl.p, "slice_calls": slice_mode,
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, all slices on-device",
+            "l2": "inputs larger than L2 (bf16 weights %.1f GB, fp32 gradients %.1f GB)"
+                  % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9)}
 
 
 def adam_oracle_sample(n=1 << 22):
@@ -215,29 +225,30 @@ def run_reference(args, wl, rank, world):
     """The CPU oracle timed on the host cores: each step is a bounded sample."""
     if rank != 0:
         return
-    import numpy as np  # noqa: F401
     from transformer_lm_megatron_gb300 import inputs as gin
     w = gin.make_weights(wl.h, wl.ffn, device="cpu") if wl.h * wl.ffn <= 64 * 2**20 else None
     if w is None:
         import torch
         w = _sample_weights_host(wl, "cuda" if torch.cuda.is_available() else "cpu")
     n_tok = args.cpu_tokens
+    sample = oracle_sample_inputs(wl, w, n_tok)
+    del w
     for _ in range(args.warmup):
-        oracle_sample(wl, w, n_tok)
+        oracle_sample(wl, sample)
     times, flops = [], 0
     for _ in range(args.steps):
-        dt, fl = oracle_sample(wl, w, n_tok)
+        dt, fl = oracle_sample(wl, sample)
         times.append(dt)
         flops = fl
     total = sum(times)
     value = flops * args.steps / total / 1e12
-    sample = f"{n_tok} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, float64, per step"
+    desc = f"{n_tok} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, float64 numpy, per step"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "tokens": wl.tokens, "h": wl.h, "ffn": wl.ffn, "t": wl.t, "k": wl.k},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle", "sample": sample},
+        "config": workload_config(wl, args.slice_mode, world),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -446,7 +457,8 @@ def run_ours(args, wl, rank, world, dist):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         w_host = tuple(x.cpu() for x in weights)
-        dt, fl = oracle_sample(wl, w_host, args.cpu_tokens)
+        dt, fl = oracle_sample(wl, oracle_sample_inputs(wl, w_host, args.cpu_tokens))
+        del w_host
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
                "sample": f"{args.cpu_tokens} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, "
                          f"float64 numpy, {dt:.1f} s"}
@@ -462,14 +474,10 @@ def run_ours(args, wl, rank, world, dist):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "pct_of_peak": 100.0 * value / (world * burst),
         "peak_tflops": {"value": burst, "kind": f"bf16 dense burst, {peaks['source']}"},
-        "config": {"workload": wl.name, "tokens": wl.tokens, "h": wl.h, "ffn": wl.ffn, "t": wl.t,
-                   "micro_batches": wl.k, "dropout": wl.p, "slice_calls": args.slice_mode,
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU, all slices on-device",
-                   "l2": "inputs larger than L2 (bf16 weights %.1f GB, fp32 gradients %.1f GB)"
-                         % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9),
-                   "grad_init": ("grad_accum_reset + every micro-batch adds (inside the timed region)"
-                                 if args.reset_each_step else
-                                 "first micro-batch of each step writes dA/da/dB/db, later ones add; no reset pass")},
+        "config": dict(workload_config(wl, args.slice_mode, world),
+                       grad_init=("grad_accum_reset + every micro-batch adds (inside the timed region)"
+                                  if args.reset_each_step else
+                                  "first micro-batch of each step writes dA/da/dB/db, later ones add; no reset pass")),
         "gpu_launches": n_launch,
         "roofline": roofline,
         "cpu_baseline": cpu,
