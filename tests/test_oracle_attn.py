@@ -1,0 +1,100 @@
+"""Pins of the attention-block oracle: torch's causal scaled_dot_product_attention
+with autograd in float64 (a library routine), slice invariance over the head split,
+and central finite differences."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attn_oracle as ato
+from oracle import mlp_oracle as orc
+
+
+def _inputs(T, h, rng, std=0.3):
+    X = orc.round_bf16(rng.standard_normal((T, h)))
+    Wqkv = orc.round_bf16(rng.standard_normal((h, 3 * h)) * std)
+    bqkv = orc.round_bf16(rng.standard_normal(3 * h) * std)
+    Wo = orc.round_bf16(rng.standard_normal((h, h)) * std)
+    bo = orc.round_bf16(rng.standard_normal(h) * std)
+    dOut = orc.round_bf16(rng.standard_normal((T, h)))
+    return X, Wqkv, bqkv, Wo, bo, dOut
+
+
+def _torch_block(X, Wqkv, bqkv, Wo, bo, keep, p, dOut, nh, seq_len):
+    T, h = X.shape
+    d = h // nh
+    n_seq = T // seq_len
+    ts = [torch.from_numpy(a.copy()).requires_grad_(True) for a in (X, Wqkv, bqkv, Wo, bo)]
+    tX, tW, tb, tWo, tbo = ts
+    qkv = torch.nn.functional.linear(tX, tW.t(), tb)
+
+    def heads(x):
+        return x.reshape(n_seq, seq_len, nh, d).transpose(1, 2)
+
+    q, k, v = heads(qkv[:, :h]), heads(qkv[:, h:2 * h]), heads(qkv[:, 2 * h:])
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    o = o.transpose(1, 2).reshape(T, h)
+    z = torch.nn.functional.linear(o, tWo.t(), tbo)
+    m = torch.from_numpy(keep.astype(np.float64)) / (1.0 - float(np.float32(p)))
+    out = tX + z * m
+    out.backward(torch.from_numpy(dOut))
+    return {"out": out.detach().numpy(), "O": o.detach().numpy(), "dX": tX.grad.numpy(), "dWqkv": tW.grad.numpy(),
+            "dbqkv": tb.grad.numpy(), "dWo": tWo.grad.numpy(), "dbo": tbo.grad.numpy()}
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_block_matches_torch_sdpa_autograd(t):
+    rng = np.random.default_rng(3)
+    T, h, nh, seq_len, p = 24, 16, 4, 12, 0.25
+    X, Wqkv, bqkv, Wo, bo, dOut = _inputs(T, h, rng)
+    fw = ato.attn_fwd(X, Wqkv, bqkv, Wo, bo, nh, t, seq_len, p, seed=5, token_offset=2)
+    bw = ato.attn_bwd(dOut, X, Wqkv, Wo, fw["QKV"], fw["P"], fw["O"], fw["keep"], nh, t, seq_len, p)
+    ref = _torch_block(X, Wqkv, bqkv, Wo, bo, fw["keep"], p, dOut, nh, seq_len)
+    np.testing.assert_allclose(fw["O"], ref["O"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(fw["out"], ref["out"], rtol=1e-11, atol=1e-12)
+    for key in ("dX", "dWqkv", "dbqkv", "dWo", "dbo"):
+        np.testing.assert_allclose(bw[key], ref[key], rtol=1e-10, atol=1e-11)
+
+
+def test_probabilities_are_causal_and_normalised():
+    rng = np.random.default_rng(4)
+    X, Wqkv, bqkv, Wo, bo, _ = _inputs(16, 8, rng)
+    fw = ato.attn_fwd(X, Wqkv, bqkv, Wo, bo, 2, 1, 8, 0.1, 1)
+    P = fw["P"]
+    np.testing.assert_allclose(P.sum(axis=-1), 1.0, rtol=1e-13)
+    assert np.all(np.triu(P, k=1) == 0)
+    assert np.all(P[..., 0, 0] == 1.0)               # the first query sees only itself
+
+
+def test_finite_differences():
+    rng = np.random.default_rng(8)
+    T, h, nh, t, seq_len, p, seed = 6, 4, 2, 2, 3, 0.25, 11
+    X, Wqkv, bqkv, Wo, bo, G = _inputs(T, h, rng, std=0.5)
+
+    def loss(X_, W_, b_, Wo_, bo_):
+        return float(np.sum(ato.attn_fwd(X_, W_, b_, Wo_, bo_, nh, t, seq_len, p, seed)["out"] * G))
+
+    fw = ato.attn_fwd(X, Wqkv, bqkv, Wo, bo, nh, t, seq_len, p, seed)
+    assert 0 < fw["keep"].sum() < fw["keep"].size
+    bw = ato.attn_bwd(G, X, Wqkv, Wo, fw["QKV"], fw["P"], fw["O"], fw["keep"], nh, t, seq_len, p)
+    args = [X, Wqkv, bqkv, Wo, bo]
+    names = ["dX", "dWqkv", "dbqkv", "dWo", "dbo"]
+    eps = 1e-6
+    for which, name in enumerate(names):
+        num = np.empty_like(args[which])
+        for idx in np.ndindex(args[which].shape):
+            plus = [a.copy() for a in args]
+            minus = [a.copy() for a in args]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            num[idx] = (loss(*plus) - loss(*minus)) / (2 * eps)
+        err = np.max(np.abs(num - bw[name])) / max(np.max(np.abs(bw[name])), 1e-30)
+        assert err <= 1e-6, (name, err)
+
+
+def test_mirror_mode_rounds_at_storage_points():
+    rng = np.random.default_rng(9)
+    X, Wqkv, bqkv, Wo, bo, dOut = _inputs(16, 16, rng)
+    fm = ato.attn_fwd(X, Wqkv, bqkv, Wo, bo, 4, 2, 8, 0.1, 1, mirror=True)
+    bm = ato.attn_bwd(dOut, X, Wqkv, Wo, fm["QKV"], fm["P"], fm["O"], fm["keep"], 4, 2, 8, 0.1, mirror=True)
+    for arr in (fm["QKV"], fm["P"], fm["O"], fm["out"], bm["dZ"], bm["dO"], bm["dQKV"], bm["dX"]):
+        np.testing.assert_array_equal(orc.round_bf16(arr), arr)
