@@ -192,6 +192,65 @@ def workload_config(wl, slice_mode, world):
                   % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9)}
 
 
+ATTN_SHAPE = dict(h=20480, nh=128, t=8, seq_len=2048, tokens=2048)
+
+
+def attn_flops(tokens, h, seq_len):
+    """Algorithmic FLOPs of one attention-block forward + backward: the QKV and
+    output projections (8 T h^2 forward, twice that backward) and the attention
+    products Q K^T and P V over full (unmasked) seq_len x seq_len blocks
+    (4 T L h forward, twice that backward)."""
+    return 24 * tokens * h * h + 12 * tokens * seq_len * h
+
+
+def attn_bench(wl, dev, stream, args):
+    import torch
+    from transformer_lm_megatron_gb300 import mlp
+    c = ATTN_SHAPE
+    h, nh, t, L, T = c["h"], c["nh"], c["t"], c["seq_len"], c["tokens"]
+    g = torch.Generator(device=dev).manual_seed(7)
+
+    def rnd(*shape, std):
+        return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
+
+    w = (rnd(h, 3 * h, std=0.02), rnd(3 * h, std=0.02), rnd(h, h, std=0.02), rnd(h, std=0.02))
+    X, dOut = rnd(T, h, std=1.0), rnd(T, h, std=1.0)
+    buf = mlp.AttnBuffers(T, h, nh, L, device=dev)
+
+    def step():
+        mlp.attn_step(h, nh, t, L, wl.p, wl.seed, w, X, dOut, buf, accumulate=False, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize(dev)
+    n = 10
+    tr = mlp.Trace(capacity=40 * n)
+    tr.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    tr.stop()
+    ms = e0.elapsed_time(e1) / n
+    if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
+        raise RuntimeError(mlp.last_error())
+    flops = attn_flops(T, h, L)
+    summ = tr.summary()
+    kernels = {mlp.TRACE_NAMES.get(k, str(k)): {"launches": v[0] // n, "ms_per_step": v[1] / n}
+               for k, v in sorted(summ.items())}
+    gemm_ms = summ.get(20, (0, 0.0, 0))[1] / n
+    out = {"shape": dict(c), "flops_per_step": flops, "ms_per_step": ms, "value": flops / (ms / 1e3) / 1e12,
+           "unit": "TFLOP/s", "gemm_ms_per_step": gemm_ms,
+           "gemm_achieved_TFLOPs": (24 * T * h * h + 12 * T * L * h) / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+           "kernels": kernels,
+           "note": "attention products counted over full seq_len x seq_len blocks (the masked half is computed)"}
+    del buf, w
+    return out
+
+
 def adam_oracle_sample(n=1 << 22):
     """The Adam oracle (float64 numpy) on 4 Mi parameters, in the same unit as the GPU figure."""
     import numpy as np
@@ -431,6 +490,12 @@ def run_ours(args, wl, rank, world, dist):
                 "hyper": {k: v for k, v in hp.items()}}
         del masters, ms_state, vs_state
 
+    # ---- next row: the tensor-sliced self-attention block at the MT-NLG layer
+    # shape (h 20480, 128 heads, t 8, one 2048-token sequence), forward + backward
+    attn = None
+    if not args.no_attn and wl.name == "mtnlg":
+        attn = attn_bench(wl, dev, stream, args)
+
     # ---- HBM-bound kernels: the reset pass (R0) is not part of a step when the
     # first micro-batch writes the gradients, so it is traced here on its own.
     reset_ms = None
@@ -483,7 +548,7 @@ def run_ours(args, wl, rank, world, dist):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clock_info,
-        "next_rows": {"adam_step": adam},
+        "next_rows": {"adam_step": adam, "attn_block": attn},
     }
     print(json.dumps(line), flush=True)
 
@@ -501,6 +566,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", dest="trace", action="store_false")
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
+    ap.add_argument("--no-attn", action="store_true", help="skip the attention-block measurement")
     ap.add_argument("--reset-each-step", action="store_true",
                     help="time grad_accum_reset + all micro-batches adding, instead of the first writing")
     args = ap.parse_args()

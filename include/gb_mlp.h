@@ -147,6 +147,47 @@ int adam_step(int64_t n, const float* grad, float grad_scale, float* master, flo
               float lr, float beta1, float beta2, float eps, float weight_decay, int step, void* stream);
 
 /*
+ * attn_fwd - forward of the tensor-sliced self-attention block (the next row after
+ * the MLP block).  The pages give the model as a left-to-right decoder with 128
+ * heads trained with Megatron tensor slicing (jiqizhixin article on MT-NLG; MT-NLG
+ * summary page); they spell the split out only for the MLP ("STRONGHOLD" slides,
+ * items 7-8).  Reading, mirroring it: the fused QKV projection is split
+ * column-wise by heads, each head attends causally within its sequence, and the
+ * output projection is split row-wise with the partial products summed over
+ * slices (operator g), then bias, dropout and residual as in the MLP block:
+ *   QKV = X Wqkv + bqkv;  per sequence and head: P = softmax(mask(Q K^T / sqrt(d))),
+ *   O_head = P V;  out = R + dropout(O Wo + bo)        (the MLP block's dropout mask)
+ * All t slices run in every call; each launch covers every head, and the sum over
+ * slices of O_i Wo_i forms in the fp32 accumulator.
+ *   h = hidden, nh = heads (d = h / nh, d % 8 == 0), t | nh, tokens = n_seq * seq_len,
+ *   seq_len % 8 == 0.
+ *   X, R, O, out [tokens, h]; Wqkv [h, 3h] = [Wq | Wk | Wv] with head j at columns
+ *   j*d .. (j+1)*d of each block; bqkv [3h]; Wo [h, h]; bo [h]  (bf16).
+ *   QKV [tokens, 3h] bf16 (saved), P [n_seq, nh, seq_len, seq_len] bf16 (saved
+ *   probabilities), O [tokens, h] bf16 (saved), S: fp32 workspace of P's shape.
+ * Returns MLP_OK or an error code.
+ */
+int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
+             const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* bqkv, const mlp_bf16* Wo, const mlp_bf16* bo,
+             const mlp_bf16* R, mlp_bf16* QKV, float* S, mlp_bf16* P, mlp_bf16* O, mlp_bf16* out, void* stream);
+
+/*
+ * attn_bwd - backward of the attention block; dWqkv, dbqkv, dWo, dbo (fp32) are
+ * added to (accumulate = 1) or overwritten (accumulate = 0), as in mlp_bwd:
+ *   dZ = dOut m / (1-p); dbo = sum dZ; dWo = O^T dZ; dO = dZ Wo^T;
+ *   per sequence and head: dV = P^T dO; dP = dO V^T; dS = P (dP - rowsum(dP P)) / sqrt(d);
+ *   dQ = dS K; dK = dS^T Q;  dWqkv = X^T dQKV; dbqkv = sum dQKV;
+ *   dX = [dOut +] dQKV Wqkv^T   (operator f; residual_grad selects the dOut term)
+ * dZ, dO [tokens, h] and dS (P's shape) are bf16 workspaces, dP an fp32 workspace of
+ * P's shape, dQKV [tokens, 3h] bf16, dX [tokens, h] bf16.  Returns MLP_OK or an error.
+ */
+int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
+             int residual_grad, int accumulate, const mlp_bf16* dOut, const mlp_bf16* X, const mlp_bf16* Wqkv,
+             const mlp_bf16* Wo, const mlp_bf16* QKV, const mlp_bf16* P, const mlp_bf16* O, mlp_bf16* dZ,
+             mlp_bf16* dO, float* dP, mlp_bf16* dS, mlp_bf16* dQKV, mlp_bf16* dX, float* dWqkv, float* dbqkv,
+             float* dWo, float* dbo, void* stream);
+
+/*
  * mlp_sync_status - synchronise `stream`, then return and clear the device status
  * word: MLP_OK, or MLP_ETIMEOUT if a kernel gave up on a bounded wait since the
  * last call (mlp_last_error() then names the wait), or MLP_ECUDA.
@@ -202,8 +243,8 @@ int mlp_trace_begin(int capacity);
  * mlp_trace_end - stop tracing, wait for the traced launches and report up to
  * max_entries of them in launch order: kinds[i] (0..5 = the GEMMs F1, F2, B2, B3,
  * B4, B5 of the forward/backward; 10 = dropout backward + db; 11 = column sum
- * for da; 12 = accumulator reset; 14 = adam_step), mnk[3i..3i+2] = the launch's
- * M, N, K (GEMMs)
+ * for da; 12 = accumulator reset; 14 = adam_step; 20 = attention GEMMs; 21 =
+ * softmax forward / backward), mnk[3i..3i+2] = the launch's M, N, K (GEMMs)
  * or rows, columns, 0, and ms[i] = its device time in milliseconds.  Any output
  * pointer may be NULL.  Returns the number of entries written, or an error code.
  */

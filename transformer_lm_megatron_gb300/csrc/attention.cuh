@@ -1,0 +1,109 @@
+// Row-wise softmax kernels of the attention core (HBM-bound).
+//
+// Forward:  P[r, :] = softmax(S[r, :]) for scores S (fp32) that already carry the
+//           1/sqrt(d) scale and -inf above the causal diagonal; P is stored bf16.
+// Backward: dS[r, :] = P (dP - sum_j dP_j P_j) * alpha, with alpha = 1/sqrt(d);
+//           dS is stored bf16.
+// One CTA per row (grid-stride over rows); rows of `cols` elements, cols % 8 == 0.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace gbmlp {
+
+constexpr int kSoftmaxThreads = 256;
+
+__device__ __forceinline__ float block_reduce_max(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = (l < kSoftmaxThreads / 32) ? red[l] : -INFINITY;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Fixed-order block sum (deterministic).
+__device__ __forceinline__ float block_reduce_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  v = (l < kSoftmaxThreads / 32) ? red[l] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kSoftmaxThreads)
+    k_softmax_rows(const float* __restrict__ S, uint16_t* __restrict__ P, int64_t rows, int cols) {
+  __shared__ float red[kSoftmaxThreads / 32];
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const float* s = S + r * cols;
+    uint16_t* p = P + r * cols;
+    float mx = -INFINITY;
+    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      const float4 a = reinterpret_cast<const float4*>(s + c)[0];
+      const float4 b = reinterpret_cast<const float4*>(s + c)[1];
+      mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w))));
+    }
+    mx = block_reduce_max(mx, red);
+    float sum = 0.0f;
+    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      const float4 a = reinterpret_cast<const float4*>(s + c)[0];
+      const float4 b = reinterpret_cast<const float4*>(s + c)[1];
+      sum += __expf(a.x - mx) + __expf(a.y - mx) + __expf(a.z - mx) + __expf(a.w - mx) + __expf(b.x - mx) +
+             __expf(b.y - mx) + __expf(b.z - mx) + __expf(b.w - mx);
+    }
+    sum = block_reduce_sum(sum, red);
+    const float inv = 1.0f / sum;
+    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      const float4 a = reinterpret_cast<const float4*>(s + c)[0];
+      const float4 b = reinterpret_cast<const float4*>(s + c)[1];
+      uint4 o;
+      o.x = pack_bf16x2(__expf(a.x - mx) * inv, __expf(a.y - mx) * inv);
+      o.y = pack_bf16x2(__expf(a.z - mx) * inv, __expf(a.w - mx) * inv);
+      o.z = pack_bf16x2(__expf(b.x - mx) * inv, __expf(b.y - mx) * inv);
+      o.w = pack_bf16x2(__expf(b.z - mx) * inv, __expf(b.w - mx) * inv);
+      *reinterpret_cast<uint4*>(p + c) = o;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kSoftmaxThreads)
+    k_softmax_bwd_rows(const uint16_t* __restrict__ P, const float* __restrict__ dP, uint16_t* __restrict__ dS,
+                       int64_t rows, int cols, float alpha) {
+  __shared__ float red[kSoftmaxThreads / 32];
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+    const uint16_t* p = P + r * cols;
+    const float* g = dP + r * cols;
+    float dot = 0.0f;
+    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      const uint4 q = *reinterpret_cast<const uint4*>(p + c);
+      const float4 a = reinterpret_cast<const float4*>(g + c)[0];
+      const float4 b = reinterpret_cast<const float4*>(g + c)[1];
+      dot += bf16lo(q.x) * a.x + bf16hi(q.x) * a.y + bf16lo(q.y) * a.z + bf16hi(q.y) * a.w + bf16lo(q.z) * b.x +
+             bf16hi(q.z) * b.y + bf16lo(q.w) * b.z + bf16hi(q.w) * b.w;
+    }
+    const float delta = block_reduce_sum(dot, red);
+    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      const uint4 q = *reinterpret_cast<const uint4*>(p + c);
+      const float4 a = reinterpret_cast<const float4*>(g + c)[0];
+      const float4 b = reinterpret_cast<const float4*>(g + c)[1];
+      uint4 o;
+      o.x = pack_bf16x2(bf16lo(q.x) * (a.x - delta) * alpha, bf16hi(q.x) * (a.y - delta) * alpha);
+      o.y = pack_bf16x2(bf16lo(q.y) * (a.z - delta) * alpha, bf16hi(q.y) * (a.w - delta) * alpha);
+      o.z = pack_bf16x2(bf16lo(q.z) * (b.x - delta) * alpha, bf16hi(q.z) * (b.y - delta) * alpha);
+      o.w = pack_bf16x2(bf16lo(q.w) * (b.z - delta) * alpha, bf16hi(q.w) * (b.w - delta) * alpha);
+      *reinterpret_cast<uint4*>(dS + r * cols + c) = o;
+    }
+  }
+}
+
+}  // namespace gbmlp

@@ -25,6 +25,7 @@
 #include <cuda_runtime.h>
 
 #include "adam.cuh"
+#include "attention.cuh"
 #include "elementwise.cuh"
 #include "gb_mlp.h"
 #include "gemm_tc.cuh"
@@ -57,7 +58,8 @@ TraceState g_trace;
 // Kernel identifiers reported by the trace.
 enum TraceKind {
   kTraceF1 = 0, kTraceF2 = 1, kTraceB2 = 2, kTraceB3 = 3, kTraceB4 = 4, kTraceB5 = 5,
-  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13, kTraceAdam = 14
+  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13, kTraceAdam = 14,
+  kTraceAttnGemm = 20, kTraceSoftmax = 21
 };
 
 // Records the start event of the next launch; returns its slot or -1.
@@ -92,8 +94,8 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;
-  bool gemm_attr[8] = {};   // per GEMM instantiation: dynamic smem attribute set
-  int max_pairs[8] = {};    // per CTA-pair instantiation: co-resident clusters of two
+  bool gemm_attr[16] = {};  // per GEMM instantiation: dynamic smem attribute set
+  int max_pairs[16] = {};   // per CTA-pair instantiation: co-resident clusters of two
 };
 
 
@@ -354,6 +356,30 @@ int grad_accum_reset(int h, int ffn, float* dA, float* da, float* dB, float* db,
   return MLP_OK;
 }
 
+int check_attn_shape(int h, int nh, int t, int64_t tokens, int seq_len, float p) {
+  if (h <= 0 || h % 8 != 0) return fail(MLP_EINVAL, "attention: h = %d must be a positive multiple of 8", h);
+  if (nh <= 0 || h % nh != 0 || (h / nh) % 8 != 0)
+    return fail(MLP_EINVAL, "attention: head size h / nh must be a whole multiple of 8 (h %d, nh %d)", h, nh);
+  if (t <= 0 || nh % t != 0) return fail(MLP_EINVAL, "attention: nh = %d must be a multiple of t = %d", nh, t);
+  if (seq_len <= 0 || seq_len % 8 != 0) return fail(MLP_EINVAL, "attention: seq_len = %d must be a multiple of 8", seq_len);
+  if (tokens <= 0 || tokens >= (int64_t)1 << 31 || tokens % seq_len != 0)
+    return fail(MLP_EINVAL, "attention: tokens = %lld must be a positive multiple of seq_len", (long long)tokens);
+  if (!(p >= 0.0f && p < 1.0f)) return fail(MLP_EINVAL, "attention: dropout p = %g not in [0, 1)", (double)p);
+  return MLP_OK;
+}
+
+int softmax_launch(DeviceState* st, bool backward, const uint16_t* P_in, const float* F_in, uint16_t* out, int64_t rows,
+                   int cols, float alpha, cudaStream_t s) {
+  int64_t blocks = rows < (int64_t)st->sms * 16 ? rows : (int64_t)st->sms * 16;
+  const int ts = trace_pre(s);
+  if (backward)
+    k_softmax_bwd_rows<<<(int)blocks, kSoftmaxThreads, 0, s>>>(P_in, F_in, out, rows, cols, alpha);
+  else
+    k_softmax_rows<<<(int)blocks, kSoftmaxThreads, 0, s>>>(F_in, out, rows, cols);
+  trace_post(ts, s, kTraceSoftmax, rows, cols, 0);
+  return launch_check(backward ? "softmax backward" : "softmax");
+}
+
 int adam_step(int64_t n, const float* grad, float grad_scale, float* master, float* m, float* v, mlp_bf16* weight,
               float lr, float beta1, float beta2, float eps, float weight_decay, int step, void* stream) {
   if (n <= 0) return fail(MLP_EINVAL, "adam_step: n = %lld must be positive", (long long)n);
@@ -389,6 +415,137 @@ int adam_step(int64_t n, const float* grad, float grad_scale, float* master, flo
   k_adam_step<<<(int)blocks, 256, 0, s>>>(n, grad, master, m, v, weight, p);
   trace_post(ts, s, kTraceAdam, n, 0, 0);
   return launch_check("adam_step");
+}
+
+int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
+             const mlp_bf16* X, const mlp_bf16* Wqkv, const mlp_bf16* bqkv, const mlp_bf16* Wo, const mlp_bf16* bo,
+             const mlp_bf16* R, mlp_bf16* QKV, float* S, mlp_bf16* P, mlp_bf16* O, mlp_bf16* out, void* stream) {
+  int rc = check_attn_shape(h, nh, t, tokens, seq_len, p);
+  if (rc) return rc;
+  rc = check_ptrs("attn_fwd", {X, Wqkv, bqkv, Wo, bo, QKV, S, P, O, out});
+  if (rc) return rc;
+  if (R != nullptr && !aligned16(R)) return fail(MLP_EALIGN, "attn_fwd: R is not 16-byte aligned");
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (R == nullptr) R = X;
+  const int T = (int)tokens, d = h / nh, L = seq_len, ns = T / L;
+  const int64_t h3 = 3 * (int64_t)h, LL = (int64_t)L * L;
+  // QKV = X Wqkv + bqkv: every slice's heads in one launch (column split of Wqkv)
+  EpiParams e{};
+  e.kind = kEpiBias;
+  e.ld = h3;
+  e.out0 = QKV;
+  e.bias = bqkv;
+  rc = gemm(st, X, false, h, Wqkv, true, h3, T, (int)h3, h, e, s, kTraceAttnGemm);
+  if (rc) return rc;
+  // S = Q K^T / sqrt(d), -inf above the diagonal; per (sequence, head)
+  EpiParams es{};
+  es.kind = kEpiScaleMask;
+  es.alpha = 1.0f / std::sqrt((float)d);
+  rc = gemm_batched(st, {QKV, false, L, d, h3, d, L * h3}, {QKV + h, false, L, d, h3, d, L * h3},
+                    {S, L, L, L, LL, nh * LL}, L, L, d, nh, ns, es, s, kTraceAttnGemm);
+  if (rc) return rc;
+  rc = softmax_launch(st, false, nullptr, S, P, (int64_t)ns * nh * L, L, 0.0f, s);
+  if (rc) return rc;
+  // O = P V per head, written into head j's columns of O
+  EpiParams eo{};
+  eo.kind = kEpiStore;
+  rc = gemm_batched(st, {P, false, L, L, L, LL, nh * LL}, {QKV + 2 * h, true, d, L, h3, d, L * h3},
+                    {O, d, L, h, d, (int64_t)L * h}, L, d, L, nh, ns, eo, s, kTraceAttnGemm);
+  if (rc) return rc;
+  // out = R + dropout(O Wo + bo): the row split of Wo summed over slices in the accumulator
+  EpiParams ez{};
+  ez.kind = kEpiDropRes;
+  ez.ld = h;
+  ez.in0 = R;
+  ez.bias = bo;
+  ez.out0 = out;
+  ez.drop = make_dropout(p, seed, token_offset, h);
+  return gemm(st, O, false, h, Wo, true, h, T, h, h, ez, s, kTraceAttnGemm);
+}
+
+int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
+             int residual_grad, int accumulate, const mlp_bf16* dOut, const mlp_bf16* X, const mlp_bf16* Wqkv,
+             const mlp_bf16* Wo, const mlp_bf16* QKV, const mlp_bf16* P, const mlp_bf16* O, mlp_bf16* dZ,
+             mlp_bf16* dO, float* dP, mlp_bf16* dS, mlp_bf16* dQKV, mlp_bf16* dX, float* dWqkv, float* dbqkv,
+             float* dWo, float* dbo, void* stream) {
+  int rc = check_attn_shape(h, nh, t, tokens, seq_len, p);
+  if (rc) return rc;
+  rc = check_ptrs("attn_bwd", {dOut, X, Wqkv, Wo, QKV, P, O, dZ, dO, dP, dS, dQKV, dX, dWqkv, dbqkv, dWo, dbo});
+  if (rc) return rc;
+  DeviceState* st = nullptr;
+  rc = device_state(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int T = (int)tokens, d = h / nh, L = seq_len, ns = T / L;
+  const int64_t h3 = 3 * (int64_t)h, LL = (int64_t)L * L;
+  const int acc = accumulate ? 1 : 0;
+  // dZ = dropout'(dOut), dbo (+)= sum dZ
+  {
+    const DropoutParams drop = make_dropout(p, seed, token_offset, h);
+    const int ts = trace_pre(s);
+    k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dOut, dZ, dbo, tokens, h, drop,
+                                                                                      acc);
+    trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
+    rc = launch_check("dropout backward");
+    if (rc) return rc;
+  }
+  // dWo (+)= O^T dZ
+  EpiParams ew{};
+  ew.kind = acc ? kEpiF32Add : kEpiF32Store;
+  ew.ld = h;
+  ew.g_out = dWo;
+  rc = gemm(st, O, true, h, dZ, true, h, h, h, T, ew, s, kTraceAttnGemm);
+  if (rc) return rc;
+  // dO = dZ Wo^T
+  EpiParams ed{};
+  ed.kind = kEpiStore;
+  ed.ld = h;
+  ed.out0 = dO;
+  rc = gemm(st, dZ, false, h, Wo, false, h, T, h, h, ed, s, kTraceAttnGemm);
+  if (rc) return rc;
+  // per (sequence, head): dV = P^T dO, dP = dO V^T, dS = softmax'(P, dP) / sqrt(d), dQ = dS K, dK = dS^T Q
+  EpiParams est{};
+  est.kind = kEpiStore;
+  rc = gemm_batched(st, {P, true, L, L, L, LL, nh * LL}, {dO, true, d, L, h, d, (int64_t)L * h},
+                    {dQKV + 2 * h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm);
+  if (rc) return rc;
+  EpiParams ef{};
+  ef.kind = kEpiF32Store;
+  rc = gemm_batched(st, {dO, false, L, d, h, d, (int64_t)L * h}, {QKV + 2 * h, false, L, d, h3, d, L * h3},
+                    {dP, L, L, L, LL, nh * LL}, L, L, d, nh, ns, ef, s, kTraceAttnGemm);
+  if (rc) return rc;
+  rc = softmax_launch(st, true, P, dP, dS, (int64_t)ns * nh * L, L, 1.0f / std::sqrt((float)d), s);
+  if (rc) return rc;
+  rc = gemm_batched(st, {dS, false, L, L, L, LL, nh * LL}, {QKV + h, true, d, L, h3, d, L * h3},
+                    {dQKV, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm);
+  if (rc) return rc;
+  rc = gemm_batched(st, {dS, true, L, L, L, LL, nh * LL}, {QKV, true, d, L, h3, d, L * h3},
+                    {dQKV + h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm);
+  if (rc) return rc;
+  // dbqkv (+)= sum dQKV; dWqkv (+)= X^T dQKV; dX = [dOut +] dQKV Wqkv^T
+  {
+    const int ts = trace_pre(s);
+    k_colsum_bf16<<<(int)((h3 + kColsPerCta - 1) / kColsPerCta), kColThreads, 0, s>>>(dQKV, h3, dbqkv, tokens,
+                                                                                       (int)h3, acc);
+    trace_post(ts, s, kTraceColsum, tokens, h3, 0);
+    rc = launch_check("bias-gradient column sum");
+    if (rc) return rc;
+  }
+  EpiParams eq{};
+  eq.kind = acc ? kEpiF32Add : kEpiF32Store;
+  eq.ld = h3;
+  eq.g_out = dWqkv;
+  rc = gemm(st, X, true, h, dQKV, true, h3, h, (int)h3, T, eq, s, kTraceAttnGemm);
+  if (rc) return rc;
+  EpiParams ex{};
+  ex.kind = kEpiResAdd;
+  ex.ld = h;
+  ex.in0 = residual_grad ? dOut : nullptr;
+  ex.out0 = dX;
+  return gemm(st, dQKV, false, h3, Wqkv, false, h3, T, h, (int)h3, ex, s, kTraceAttnGemm);
 }
 
 int mlp_sync_status(void* stream) {

@@ -71,13 +71,14 @@ int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int
   return make_map(m, base, k, mn, ld, kBK, tile_mn);
 }
 
-template <bool AM, bool BM, bool PAIR>
+template <bool AM, bool BM, bool PAIR, bool BATCHED = false>
 int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                   const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
-                  int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind) {
+                  int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind, int batch = 1,
+                  int nb_h = 1) {
   using Cfg = GemmCfg<PAIR>;
-  auto kern = k_gemm_bf16_tc<AM, BM, PAIR>;
-  const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0);
+  auto kern = k_gemm_bf16_tc<AM, BM, PAIR, BATCHED>;
+  const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0) + (BATCHED ? 8 : 0);
   if (!st->gemm_attr[slot]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemBytes);
     if (e != cudaSuccess) return fail(MLP_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -104,7 +105,7 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
     }
     st->gemm_attr[slot] = true;
   }
-  const int64_t tiles = (int64_t)((M + Cfg::kTileM - 1) / Cfg::kTileM) * ((N + kBN - 1) / kBN);
+  const int64_t tiles = (int64_t)((M + Cfg::kTileM - 1) / Cfg::kTileM) * ((N + kBN - 1) / kBN) * batch;
   const int ts = trace_pre(stream);
   cudaError_t e;
   if (PAIR) {
@@ -121,12 +122,12 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group, l2_hints,
-                           st->status);
+    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group, l2_hints, batch,
+                           nb_h, st->status);
   } else {
     const int grid = (int)(tiles < st->sms ? tiles : st->sms);
     kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                          group, l2_hints, st->status);
+                                                          group, l2_hints, batch, nb_h, st->status);
     e = cudaGetLastError();
   }
   trace_post(ts, stream, trace_kind, M, N, K);
@@ -149,7 +150,7 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
   memset(&mC, 0, sizeof(mC));
   memset(&mO0, 0, sizeof(mO0));
   memset(&mO1, 0, sizeof(mO1));
-  if (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add) {
+  if (epi_f32_out(ep.kind)) {
     rc = make_out_map(&mC, ep.g_out, N, M, ep.ld);
     if (rc) return rc;
   } else {
@@ -194,3 +195,87 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 
+
+// ---------------------------------------------------------------- batched GEMMs
+// One operand of a batched GEMM: matrix (b_h, b_s) of a 4-D layout.  `mn` and `k`
+// are the extents along M (or N) and the reduction; `ld` is the element distance
+// between consecutive rows of the stored matrix (rows run along K for an
+// MN-major operand, along M/N for a K-major one); h_stride / s_stride are the
+// element distances between consecutive matrices along the two batch indices.
+struct BatchOperand {
+  const void* base;
+  bool mn_major;
+  int64_t mn, k, ld, h_stride, s_stride;
+};
+
+// One output of a batched GEMM: `cols` = N, `rows` = M of each matrix.
+struct BatchOutput {
+  void* base;
+  int64_t cols, rows, ld, h_stride, s_stride;
+};
+
+int make_map4(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base, int64_t inner, int64_t rows,
+              int64_t ld, int64_t nb_h, int64_t h_stride, int64_t nb_s, int64_t s_stride, uint32_t box_inner,
+              uint32_t box_rows, CUtensorMapSwizzle swizzle, CUtensorMapL2promotion prom) {
+  cuuint64_t dims[4] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)nb_h, (cuuint64_t)nb_s};
+  cuuint64_t strides[3] = {(cuuint64_t)(ld * esz), (cuuint64_t)(h_stride * esz), (cuuint64_t)(s_stride * esz)};
+  cuuint32_t box[4] = {box_inner, box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, dt, 4, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle, prom, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MLP_ECUDA, "cuTensorMapEncodeTiled (4-D) failed (%d): inner %lld rows %lld ld %lld strides %lld %lld",
+                (int)r, (long long)inner, (long long)rows, (long long)ld, (long long)h_stride, (long long)s_stride);
+  return MLP_OK;
+}
+
+// nb_h x nb_s independent GEMMs D_b = A_b B_b (M x N, reduction K) with a
+// TMA-only epilogue (kEpiStore: bf16 output; kEpiF32Store / kEpiScaleMask: fp32).
+int gemm_batched(DeviceState* st, const BatchOperand& a, const BatchOperand& b, const BatchOutput& out, int M, int N,
+                 int K, int nb_h, int nb_s, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+  if (!epi_tma_only(ep.kind) || ep.kind == kEpiF32Add)
+    return fail(MLP_EUNSUPPORTED, "batched GEMM: epilogue kind %d not supported", ep.kind);
+  const int mode = g_pair_mode.load(std::memory_order_relaxed);
+  const bool pair = mode == 1 || (mode < 0 && M > kBM);
+  const uint32_t b_tile = pair ? GemmCfg<true>::kBLoadN : GemmCfg<false>::kBLoadN;
+  CUtensorMap mA, mB, mC, mO0, mO1;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int rc = a.mn_major ? make_map4(&mA, bf, 2, a.base, a.mn, a.k, a.ld, nb_h, a.h_stride, nb_s, a.s_stride, 64, kBK,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                      : make_map4(&mA, bf, 2, a.base, a.k, a.mn, a.ld, nb_h, a.h_stride, nb_s, a.s_stride, kBK, kBM,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  rc = b.mn_major ? make_map4(&mB, bf, 2, b.base, b.mn, b.k, b.ld, nb_h, b.h_stride, nb_s, b.s_stride, 64, kBK,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)
+                  : make_map4(&mB, bf, 2, b.base, b.k, b.mn, b.ld, nb_h, b.h_stride, nb_s, b.s_stride, kBK, b_tile,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (rc) return rc;
+  memset(&mC, 0, sizeof(mC));
+  memset(&mO0, 0, sizeof(mO0));
+  memset(&mO1, 0, sizeof(mO1));
+  if (epi_f32_out(ep.kind))
+    rc = make_map4(&mC, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, out.base, out.cols, out.rows, out.ld, nb_h, out.h_stride,
+                   nb_s, out.s_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  else
+    rc = make_map4(&mO0, bf, 2, out.base, out.cols, out.rows, out.ld, nb_h, out.h_stride, nb_s, out.s_stride, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (rc) return rc;
+  const int raster_n_fast = M > N ? 1 : 0;
+  const int batch = nb_h * nb_s;
+  if (!a.mn_major && b.mn_major)
+    return pair ? launch_gemm_t<false, true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
+                                                         stream, trace_kind, batch, nb_h)
+                : launch_gemm_t<false, true, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
+                                                          stream, trace_kind, batch, nb_h);
+  if (!a.mn_major && !b.mn_major)
+    return pair ? launch_gemm_t<false, false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
+                                                          stream, trace_kind, batch, nb_h)
+                : launch_gemm_t<false, false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
+                                                           stream, trace_kind, batch, nb_h);
+  if (a.mn_major && b.mn_major)
+    return pair ? launch_gemm_t<true, true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
+                                                        stream, trace_kind, batch, nb_h)
+                : launch_gemm_t<true, true, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
+                                                         stream, trace_kind, batch, nb_h);
+  return fail(MLP_EUNSUPPORTED, "batched GEMM: operand layout combination not instantiated");
+}

@@ -67,7 +67,19 @@ enum EpiKind : int {
   kEpiDropRes = 3,   // O = R + dropout((G ? G : 0) + acc + bias) (bf16)
   kEpiDGelu = 4,     // dU = acc * GeLU'(U) (bf16)
   kEpiResAdd = 5,    // dX = (G ? G : 0) + acc + (R ? R : 0) (bf16)
+  kEpiBias = 6,      // out = acc + bias (bf16)
+  kEpiStore = 7,     // out = acc (bf16)
+  kEpiScaleMask = 8  // G = (column > row ? -inf : alpha * acc) (fp32; causal attention scores)
 };
+
+// Epilogues whose output is fp32 (written through the fp32 TMA map tmC).
+__host__ __device__ constexpr bool epi_f32_out(int kind) {
+  return kind == kEpiF32Store || kind == kEpiF32Add || kind == kEpiScaleMask;
+}
+// Epilogues that read no tensor through plain pointers (usable in batched GEMMs).
+__host__ __device__ constexpr bool epi_tma_only(int kind) {
+  return epi_f32_out(kind) || kind == kEpiStore;
+}
 
 struct EpiParams {
   int kind;
@@ -78,6 +90,7 @@ struct EpiParams {
   uint16_t* out1;             // bf16 output: Y
   const uint16_t* in0;        // bf16 input: R (DropRes, ResAdd) or U (DGelu); may be null for ResAdd
   const uint16_t* bias;       // bias vector indexed by output column
+  float alpha;                // scale of kEpiScaleMask
   DropoutParams drop;
 };
 
@@ -148,6 +161,14 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row
       for (int j = 0; j < 8; ++j) v[j] *= gelu_prime_f(u[j]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+    } else if constexpr (KIND == kEpiBias) {
+      float bb[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      if (col_ok) ld_bf16x8(ep.bias + col, bb);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j] + bb[2 * j], v[2 * j + 1] + bb[2 * j + 1]);
+    } else if constexpr (KIND == kEpiStore) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     } else {  // kEpiResAdd
       if (ok && ep.g_in != nullptr) {
         float z[8];
@@ -173,6 +194,8 @@ __device__ __forceinline__ void epilogue_dispatch(const EpiParams& ep, int64_t r
     case kEpiGelu: epilogue_values<kEpiGelu>(ep, row, col0, r, M, N, o0, o1); break;
     case kEpiDropRes: epilogue_values<kEpiDropRes>(ep, row, col0, r, M, N, o0, o1); break;
     case kEpiDGelu: epilogue_values<kEpiDGelu>(ep, row, col0, r, M, N, o0, o1); break;
+    case kEpiBias: epilogue_values<kEpiBias>(ep, row, col0, r, M, N, o0, o1); break;
+    case kEpiStore: epilogue_values<kEpiStore>(ep, row, col0, r, M, N, o0, o1); break;
     default: epilogue_values<kEpiResAdd>(ep, row, col0, r, M, N, o0, o1); break;
   }
 }
@@ -195,12 +218,14 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // while the larger operand streams past them.
 // l2_hints: L2 policy of the A loads (bits 0-1), the B loads (bits 2-3) and the
 // output stores (bits 4-5), an L2Hint each (kL2None: no hint).
-template <bool A_MN, bool B_MN, bool PAIR>
+// BATCHED: `batch` independent GEMMs of the same M, N, K; every tensor map is 4-D
+// (x, y, hb, sb) with batch b = sb * nb_h + hb; only TMA-only epilogues.
+template <bool A_MN, bool B_MN, bool PAIR, bool BATCHED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
-                   int group, int l2_hints, int* status) {
+                   int group, int l2_hints, int batch, int nb_h, int* status) {
   using Cfg = GemmCfg<PAIR>;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -222,7 +247,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const int num_m = (M + Cfg::kTileM - 1) / Cfg::kTileM;
   const int num_n = (N + kBN - 1) / kBN;
-  const int num_tiles = num_m * num_n;
+  const int tiles_per_batch = num_m * num_n;
+  const int num_tiles = tiles_per_batch * (BATCHED ? batch : 1);
   const int num_kb = (K + kBK - 1) / kBK;
 
   // A pipeline that broke in an earlier launch leaves the status word set; later
@@ -241,7 +267,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     mbar_init(mma_done, 1);
     fence_mbar_init();
   }
-  const bool tma_out = (ep.kind == kEpiF32Store || ep.kind == kEpiF32Add);
+  const bool tma_out = epi_f32_out(ep.kind);
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
@@ -273,7 +299,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
   const int tile_end = skip ? 0 : num_tiles;
 
-  auto tile_origin = [&](int tile, int& m0, int& n0) {
+  auto tile_origin = [&](int tile, int& m0, int& n0, int& hb, int& sb) {
+    hb = 0;
+    sb = 0;
+    if constexpr (BATCHED) {
+      const int b = tile / tiles_per_batch;
+      tile -= b * tiles_per_batch;
+      hb = b % nb_h;
+      sb = b / nb_h;
+    }
     // fast: blocks along the fast dimension; slow: along the other one
     const int n_fast = raster_n_fast ? num_n : num_m;
     const int n_slow = raster_n_fast ? num_m : num_n;
@@ -302,8 +336,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int tile = unit; tile < tile_end && ok; tile += num_units) {
-        int m0, n0;
-        tile_origin(tile, m0, n0);
+        int m0, n0, hb, sb;
+        tile_origin(tile, m0, n0, hb, sb);
         const int b_n0 = n0 + (PAIR ? (int)rank * Cfg::kBLoadN : 0);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
@@ -314,7 +348,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int k0 = kb * kBK;
           uint8_t* a_dst = sA + stage * kABytes;
           uint8_t* b_dst = sB + stage * Cfg::kBBytes;
-          if constexpr (PAIR) {
+          if constexpr (BATCHED) {
+            if constexpr (PAIR) {
+              const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
+              if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
+              if constexpr (A_MN) {
+#pragma unroll
+                for (int j = 0; j < kBM / 64; ++j)
+                  tma_load_4d_pair(a_dst + j * kChunkBytes, &tmA, bar, m0 + 64 * j, k0, hb, sb);
+              } else {
+                tma_load_4d_pair(a_dst, &tmA, bar, k0, m0, hb, sb);
+              }
+              if constexpr (B_MN) {
+#pragma unroll
+                for (int j = 0; j < Cfg::kBLoadN / 64; ++j)
+                  tma_load_4d_pair(b_dst + j * kChunkBytes, &tmB, bar, b_n0 + 64 * j, k0, hb, sb);
+              } else {
+                tma_load_4d_pair(b_dst, &tmB, bar, k0, b_n0, hb, sb);
+              }
+            } else {
+              mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+              if constexpr (A_MN) {
+#pragma unroll
+                for (int j = 0; j < kBM / 64; ++j)
+                  tma_load_4d(a_dst + j * kChunkBytes, &tmA, &full[stage], m0 + 64 * j, k0, hb, sb);
+              } else {
+                tma_load_4d(a_dst, &tmA, &full[stage], k0, m0, hb, sb);
+              }
+              if constexpr (B_MN) {
+#pragma unroll
+                for (int j = 0; j < Cfg::kBLoadN / 64; ++j)
+                  tma_load_4d(b_dst + j * kChunkBytes, &tmB, &full[stage], b_n0 + 64 * j, k0, hb, sb);
+              } else {
+                tma_load_4d(b_dst, &tmB, &full[stage], k0, b_n0, hb, sb);
+              }
+            }
+          } else if constexpr (PAIR) {
             // both CTAs' copies complete on the even CTA's barrier, which expects both
             const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);
             if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * Cfg::kStageBytes);
@@ -441,8 +510,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = unit; tile < tile_end; tile += num_units) {
-      int m0, n0;
-      tile_origin(tile, m0, n0);
+      int m0, n0, hb, sb;
+      tile_origin(tile, m0, n0, hb, sb);
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
@@ -460,6 +529,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           // rows >= M and columns >= N are clipped by the tensor map.
           if (n0 + c0 < N && m0 + quarter * 32 < M) {
             uint8_t* box = my_out + (n_out & 1) * kOutBoxBytes;
+            if (ep.kind == kEpiScaleMask) {
+              // causal attention scores: key (column) after query (row) -> -inf
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float val = (n0 + c0 + j > row) ? -INFINITY : ep.alpha * __uint_as_float(r[j]);
+                r[j] = __float_as_uint(val);
+              }
+            }
             if (lane == 0) bulk_wait_read<1>();  // the box issued two rounds ago has been read
             __syncwarp();
 #pragma unroll
@@ -470,10 +547,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (ep.kind == kEpiF32Add)
-                tma_reduce_add_2d(&tmC, box, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
-              else
-                tma_store_2d(&tmC, box, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+              if constexpr (BATCHED) {
+                tma_store_4d(&tmC, box, n0 + c0, m0 + quarter * 32, hb, sb);
+              } else {
+                if (ep.kind == kEpiF32Add)
+                  tma_reduce_add_2d(&tmC, box, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+                else
+                  tma_store_2d(&tmC, box, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+              }
               bulk_commit();
             }
             ++n_out;
@@ -481,7 +562,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         } else if (n0 + c0 < N && m0 + quarter * 32 < M) {
           // Warp-uniform, as above: bf16 output box(es) of 32 rows x 32 columns.
           uint32_t o0[16], o1[16];
-          epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1);
+          if constexpr (BATCHED) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)  // kEpiStore: the only bf16 epilogue of batched GEMMs
+              o0[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          } else {
+            epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1);
+          }
           uint8_t* box0 = my_out + (n_out & 1) * (2 * kOutBoxBf16Bytes);
           uint8_t* box1 = box0 + kOutBoxBf16Bytes;
           const bool two = ep.kind == kEpiGelu;
@@ -498,8 +585,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tma_store_2d(&tmO0, box0, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
-            if (two) tma_store_2d(&tmO1, box1, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+            if constexpr (BATCHED) {
+              tma_store_4d(&tmO0, box0, n0 + c0, m0 + quarter * 32, hb, sb);
+            } else {
+              tma_store_2d(&tmO0, box0, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+              if (two) tma_store_2d(&tmO1, box1, n0 + c0, m0 + quarter * 32, pol_out, hout != kL2None);
+            }
             bulk_commit();
           }
           ++n_out;

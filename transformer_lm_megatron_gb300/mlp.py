@@ -42,6 +42,8 @@ _SIGNATURES = {
     "mlp_launch_count": (_u64, []),
     "mlp_set_cta_pair": (_i32, [_i32]),
     "adam_step": (_i32, [_i64, _vp, _f32, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i32, _vp]),
+    "attn_fwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64] + [_vp] * 11 + [_vp]),
+    "attn_bwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64, _i32, _i32] + [_vp] * 17 + [_vp]),
     "mlp_fwd_static_scratch": (_i32, [_i32, _i32, _i32, _i32, _i64, _f32, _u64, _u64] + [_vp] * 6 + [_vp, _vp, _vp, _vp]),
     "mlp_trace_begin": (_i32, [_i32]),
     "mlp_trace_end": (_i32, [_i32, _vp, _vp, _vp]),
@@ -135,6 +137,57 @@ def adam_step(grad, master, m, v, weight, lr, beta1=0.9, beta2=0.95, eps=1e-8, w
                             beta2, eps, weight_decay, step, _stream(stream)))
 
 
+def attn_fwd(h, nh, t, tokens, seq_len, p, seed, token_offset, X, Wqkv, bqkv, Wo, bo, R, QKV, S, P, O, out,
+             stream=None):
+    _check(load().attn_fwd(h, nh, t, tokens, seq_len, p, seed, token_offset, _ptr(X), _ptr(Wqkv), _ptr(bqkv),
+                           _ptr(Wo), _ptr(bo), _ptr(R), _ptr(QKV), _ptr(S), _ptr(P), _ptr(O), _ptr(out),
+                           _stream(stream)))
+
+
+def attn_bwd(h, nh, t, tokens, seq_len, p, seed, token_offset, residual_grad, accumulate, dOut, X, Wqkv, Wo, QKV, P,
+             O, dZ, dO, dP, dS, dQKV, dX, dWqkv, dbqkv, dWo, dbo, stream=None):
+    _check(load().attn_bwd(h, nh, t, tokens, seq_len, p, seed, token_offset, int(residual_grad), int(accumulate),
+                           _ptr(dOut), _ptr(X), _ptr(Wqkv), _ptr(Wo), _ptr(QKV), _ptr(P), _ptr(O), _ptr(dZ), _ptr(dO),
+                           _ptr(dP), _ptr(dS), _ptr(dQKV), _ptr(dX), _ptr(dWqkv), _ptr(dbqkv), _ptr(dWo), _ptr(dbo),
+                           _stream(stream)))
+
+
+class AttnBuffers:
+    """Saved activations, workspaces and fp32 gradients of the attention block."""
+
+    def __init__(self, tokens: int, h: int, nh: int, seq_len: int, device="cuda"):
+        n_seq = tokens // seq_len
+        bf = dict(dtype=torch.bfloat16, device=device)
+        f32 = dict(dtype=torch.float32, device=device)
+        pshape = (n_seq, nh, seq_len, seq_len)
+        self.QKV = torch.empty(tokens, 3 * h, **bf)
+        self.S = torch.empty(pshape, **f32)
+        self.P = torch.empty(pshape, **bf)
+        self.O = torch.empty(tokens, h, **bf)
+        self.out = torch.empty(tokens, h, **bf)
+        self.dZ = torch.empty(tokens, h, **bf)
+        self.dO = torch.empty(tokens, h, **bf)
+        self.dP = self.S          # the scores are dead once P exists; the backward reuses them
+        self.dS = torch.empty(pshape, **bf)
+        self.dQKV = torch.empty(tokens, 3 * h, **bf)
+        self.dX = torch.empty(tokens, h, **bf)
+        self.dWqkv = torch.zeros(h, 3 * h, **f32)
+        self.dbqkv = torch.zeros(3 * h, **f32)
+        self.dWo = torch.zeros(h, h, **f32)
+        self.dbo = torch.zeros(h, **f32)
+
+
+def attn_step(h, nh, t, seq_len, p, seed, weights, X, dOut, buf: AttnBuffers, token_offset=0, accumulate=True,
+              stream=None):
+    """One forward + backward of the attention block on one micro-batch."""
+    Wqkv, bqkv, Wo, bo = weights
+    T = X.shape[0]
+    attn_fwd(h, nh, t, T, seq_len, p, seed, token_offset, X, Wqkv, bqkv, Wo, bo, None, buf.QKV, buf.S, buf.P, buf.O,
+             buf.out, stream)
+    attn_bwd(h, nh, t, T, seq_len, p, seed, token_offset, 1, accumulate, dOut, X, Wqkv, Wo, buf.QKV, buf.P, buf.O,
+             buf.dZ, buf.dO, buf.dP, buf.dS, buf.dQKV, buf.dX, buf.dWqkv, buf.dbqkv, buf.dWo, buf.dbo, stream)
+
+
 def mlp_sync_status(stream=None) -> int:
     return load().mlp_sync_status(_stream(stream))
 
@@ -161,7 +214,8 @@ def mlp_set_cta_pair(mode: int):
 
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
                3: "B3 gemm Y_i^T.dZ (+= dB)", 4: "B4 gemm X^T.dU_i (+= dA)", 5: "B5 gemm dU_i.A_i^T (+dO)",
-               10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset", 14: "adam step"}
+               10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset", 14: "adam step",
+               20: "attention GEMM", 21: "softmax fwd/bwd"}
 GEMM_KINDS = (0, 1, 2, 3, 4, 5)
 
 
