@@ -198,9 +198,9 @@ ATTN_SHAPE = dict(h=20480, nh=128, t=8, seq_len=2048, tokens=2048)
 def attn_flops(tokens, h, seq_len):
     """Algorithmic FLOPs of one attention-block forward + backward: the QKV and
     output projections (8 T h^2 forward, twice that backward) and the attention
-    products Q K^T and P V over full (unmasked) seq_len x seq_len blocks
-    (4 T L h forward, twice that backward)."""
-    return 24 * tokens * h * h + 12 * tokens * seq_len * h
+    products over the causal lower triangle only (Q K^T and P V: 2 T L h forward;
+    dV, dP, dQ, dK: 4 T L h backward), i.e. half of the full L x L blocks."""
+    return 24 * tokens * h * h + 6 * tokens * seq_len * h
 
 
 def attn_bench(wl, dev, stream, args):
@@ -244,9 +244,10 @@ def attn_bench(wl, dev, stream, args):
     gemm_ms = summ.get(20, (0, 0.0, 0))[1] / n
     out = {"shape": dict(c), "flops_per_step": flops, "ms_per_step": ms, "value": flops / (ms / 1e3) / 1e12,
            "unit": "TFLOP/s", "gemm_ms_per_step": gemm_ms,
-           "gemm_achieved_TFLOPs": (24 * T * h * h + 12 * T * L * h) / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
+           "gemm_achieved_TFLOPs": flops / (gemm_ms / 1e3) / 1e12 if gemm_ms else None,
            "kernels": kernels,
-           "note": "attention products counted over full seq_len x seq_len blocks (the masked half is computed)"}
+           "note": "attention products counted over the causal lower triangle; tiles wholly above the diagonal "
+                   "are skipped, the rest of each diagonal tile is computed and masked"}
     del buf, w
     return out
 

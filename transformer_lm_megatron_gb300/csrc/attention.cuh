@@ -5,6 +5,10 @@
 // Backward: dS[r, :] = P (dP - sum_j dP_j P_j) * alpha, with alpha = 1/sqrt(d);
 //           dS is stored bf16.
 // One CTA per row (grid-stride over rows); rows of `cols` elements, cols % 8 == 0.
+// The rows are causal: row r is query q = r % cols of its sequence and only keys
+// c <= q carry probability.  Both kernels read the first roundup8(q + 1) entries
+// (the scores beyond q there are -inf, the gradients finite) and write exact zeros
+// for the rest of the row, so the masked half of S and dP is never read.
 #pragma once
 #include <cstdint>
 
@@ -47,15 +51,16 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const float* s = S + r * cols;
     uint16_t* p = P + r * cols;
+    const int active = ((int)(r % cols) + 8) & ~7;  // roundup8(q + 1)
     float mx = -INFINITY;
-    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+    for (int c = threadIdx.x * 8; c < active; c += kSoftmaxThreads * 8) {
       const float4 a = reinterpret_cast<const float4*>(s + c)[0];
       const float4 b = reinterpret_cast<const float4*>(s + c)[1];
       mx = fmaxf(mx, fmaxf(fmaxf(fmaxf(a.x, a.y), fmaxf(a.z, a.w)), fmaxf(fmaxf(b.x, b.y), fmaxf(b.z, b.w))));
     }
     mx = block_reduce_max(mx, red);
     float sum = 0.0f;
-    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+    for (int c = threadIdx.x * 8; c < active; c += kSoftmaxThreads * 8) {
       const float4 a = reinterpret_cast<const float4*>(s + c)[0];
       const float4 b = reinterpret_cast<const float4*>(s + c)[1];
       sum += __expf(a.x - mx) + __expf(a.y - mx) + __expf(a.z - mx) + __expf(a.w - mx) + __expf(b.x - mx) +
@@ -64,6 +69,10 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
     sum = block_reduce_sum(sum, red);
     const float inv = 1.0f / sum;
     for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      if (c >= active) {
+        *reinterpret_cast<uint4*>(p + c) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       const float4 a = reinterpret_cast<const float4*>(s + c)[0];
       const float4 b = reinterpret_cast<const float4*>(s + c)[1];
       uint4 o;
@@ -83,8 +92,9 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const uint16_t* p = P + r * cols;
     const float* g = dP + r * cols;
+    const int active = ((int)(r % cols) + 8) & ~7;  // roundup8(q + 1)
     float dot = 0.0f;
-    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+    for (int c = threadIdx.x * 8; c < active; c += kSoftmaxThreads * 8) {
       const uint4 q = *reinterpret_cast<const uint4*>(p + c);
       const float4 a = reinterpret_cast<const float4*>(g + c)[0];
       const float4 b = reinterpret_cast<const float4*>(g + c)[1];
@@ -93,6 +103,10 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
     }
     const float delta = block_reduce_sum(dot, red);
     for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
+      if (c >= active) {
+        *reinterpret_cast<uint4*>(dS + r * cols + c) = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       const uint4 q = *reinterpret_cast<const uint4*>(p + c);
       const float4 a = reinterpret_cast<const float4*>(g + c)[0];
       const float4 b = reinterpret_cast<const float4*>(g + c)[1];

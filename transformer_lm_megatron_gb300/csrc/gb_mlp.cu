@@ -445,7 +445,7 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   es.kind = kEpiScaleMask;
   es.alpha = 1.0f / std::sqrt((float)d);
   rc = gemm_batched(st, {QKV, false, L, d, h3, d, L * h3}, {QKV + h, false, L, d, h3, d, L * h3},
-                    {S, L, L, L, LL, nh * LL}, L, L, d, nh, ns, es, s, kTraceAttnGemm);
+                    {S, L, L, L, LL, nh * LL}, L, L, d, nh, ns, es, s, kTraceAttnGemm, kCausalSkipUpper);
   if (rc) return rc;
   rc = softmax_launch(st, false, nullptr, S, P, (int64_t)ns * nh * L, L, 0.0f, s);
   if (rc) return rc;
@@ -453,7 +453,7 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   EpiParams eo{};
   eo.kind = kEpiStore;
   rc = gemm_batched(st, {P, false, L, L, L, LL, nh * LL}, {QKV + 2 * h, true, d, L, h3, d, L * h3},
-                    {O, d, L, h, d, (int64_t)L * h}, L, d, L, nh, ns, eo, s, kTraceAttnGemm);
+                    {O, d, L, h, d, (int64_t)L * h}, L, d, L, nh, ns, eo, s, kTraceAttnGemm, kCausalKUpTo);
   if (rc) return rc;
   // out = R + dropout(O Wo + bo): the row split of Wo summed over slices in the accumulator
   EpiParams ez{};
@@ -510,20 +510,20 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   EpiParams est{};
   est.kind = kEpiStore;
   rc = gemm_batched(st, {P, true, L, L, L, LL, nh * LL}, {dO, true, d, L, h, d, (int64_t)L * h},
-                    {dQKV + 2 * h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm);
+                    {dQKV + 2 * h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKFrom);
   if (rc) return rc;
   EpiParams ef{};
   ef.kind = kEpiF32Store;
   rc = gemm_batched(st, {dO, false, L, d, h, d, (int64_t)L * h}, {QKV + 2 * h, false, L, d, h3, d, L * h3},
-                    {dP, L, L, L, LL, nh * LL}, L, L, d, nh, ns, ef, s, kTraceAttnGemm);
+                    {dP, L, L, L, LL, nh * LL}, L, L, d, nh, ns, ef, s, kTraceAttnGemm, kCausalSkipUpper);
   if (rc) return rc;
   rc = softmax_launch(st, true, P, dP, dS, (int64_t)ns * nh * L, L, 1.0f / std::sqrt((float)d), s);
   if (rc) return rc;
   rc = gemm_batched(st, {dS, false, L, L, L, LL, nh * LL}, {QKV + h, true, d, L, h3, d, L * h3},
-                    {dQKV, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm);
+                    {dQKV, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKUpTo);
   if (rc) return rc;
   rc = gemm_batched(st, {dS, true, L, L, L, LL, nh * LL}, {QKV, true, d, L, h3, d, L * h3},
-                    {dQKV + h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm);
+                    {dQKV + h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKFrom);
   if (rc) return rc;
   // dbqkv (+)= sum dQKV; dWqkv (+)= X^T dQKV; dX = [dOut +] dQKV Wqkv^T
   {

@@ -75,7 +75,7 @@ template <bool AM, bool BM, bool PAIR, bool BATCHED = false>
 int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                   const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
                   int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind, int batch = 1,
-                  int nb_h = 1) {
+                  int nb_h = 1, int causal = kCausalNone) {
   using Cfg = GemmCfg<PAIR>;
   auto kern = k_gemm_bf16_tc<AM, BM, PAIR, BATCHED>;
   const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0) + (BATCHED ? 8 : 0);
@@ -123,11 +123,11 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group, l2_hints, batch,
-                           nb_h, st->status);
+                           nb_h, causal, st->status);
   } else {
     const int grid = (int)(tiles < st->sms ? tiles : st->sms);
     kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                          group, l2_hints, batch, nb_h, st->status);
+                                                          group, l2_hints, batch, nb_h, causal, st->status);
     e = cudaGetLastError();
   }
   trace_post(ts, stream, trace_kind, M, N, K);
@@ -232,7 +232,8 @@ int make_map4(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
 // nb_h x nb_s independent GEMMs D_b = A_b B_b (M x N, reduction K) with a
 // TMA-only epilogue (kEpiStore: bf16 output; kEpiF32Store / kEpiScaleMask: fp32).
 int gemm_batched(DeviceState* st, const BatchOperand& a, const BatchOperand& b, const BatchOutput& out, int M, int N,
-                 int K, int nb_h, int nb_s, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+                 int K, int nb_h, int nb_s, const EpiParams& ep, cudaStream_t stream, int trace_kind,
+                 int causal = kCausalNone) {
   if (!epi_tma_only(ep.kind) || ep.kind == kEpiF32Add)
     return fail(MLP_EUNSUPPORTED, "batched GEMM: epilogue kind %d not supported", ep.kind);
   const int mode = g_pair_mode.load(std::memory_order_relaxed);
@@ -264,18 +265,18 @@ int gemm_batched(DeviceState* st, const BatchOperand& a, const BatchOperand& b, 
   const int batch = nb_h * nb_s;
   if (!a.mn_major && b.mn_major)
     return pair ? launch_gemm_t<false, true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
-                                                         stream, trace_kind, batch, nb_h)
+                                                         stream, trace_kind, batch, nb_h, causal)
                 : launch_gemm_t<false, true, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
-                                                          stream, trace_kind, batch, nb_h);
+                                                          stream, trace_kind, batch, nb_h, causal);
   if (!a.mn_major && !b.mn_major)
     return pair ? launch_gemm_t<false, false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
-                                                          stream, trace_kind, batch, nb_h)
+                                                          stream, trace_kind, batch, nb_h, causal)
                 : launch_gemm_t<false, false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
-                                                           stream, trace_kind, batch, nb_h);
+                                                           stream, trace_kind, batch, nb_h, causal);
   if (a.mn_major && b.mn_major)
     return pair ? launch_gemm_t<true, true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
-                                                        stream, trace_kind, batch, nb_h)
+                                                        stream, trace_kind, batch, nb_h, causal)
                 : launch_gemm_t<true, true, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, 0, 0,
-                                                         stream, trace_kind, batch, nb_h);
+                                                         stream, trace_kind, batch, nb_h, causal);
   return fail(MLP_EUNSUPPORTED, "batched GEMM: operand layout combination not instantiated");
 }

@@ -60,6 +60,8 @@ struct GemmCfg {
 };
 static_assert(GemmCfg<true>::kSmemBytes <= 232448 && GemmCfg<false>::kSmemBytes <= 232448, "smem budget");
 
+enum CausalMode : int { kCausalNone = 0, kCausalSkipUpper = 1, kCausalKUpTo = 2, kCausalKFrom = 3 };
+
 enum EpiKind : int {
   kEpiGelu = 0,      // U = acc + bias (bf16), Y = GeLU(acc + bias) (bf16)
   kEpiF32Store = 1,  // G = acc (fp32)
@@ -220,12 +222,17 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // output stores (bits 4-5), an L2Hint each (kL2None: no hint).
 // BATCHED: `batch` independent GEMMs of the same M, N, K; every tensor map is 4-D
 // (x, y, hb, sb) with batch b = sb * nb_h + hb; only TMA-only epilogues.
+// causal (batched attention products, M and N or K indexing positions in one
+// sequence): kCausalNone; kCausalSkipUpper skips tiles whose columns all lie
+// after the tile's last row (the result there is never read); kCausalKUpTo stops
+// each tile's reduction after its last row (A(m, k) = 0 for k > m);
+// kCausalKFrom starts it at the tile's first row (A(m, k) = 0 for k < m).
 template <bool A_MN, bool B_MN, bool PAIR, bool BATCHED>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
-                   int group, int l2_hints, int batch, int nb_h, int* status) {
+                   int group, int l2_hints, int batch, int nb_h, int causal, int* status) {
   using Cfg = GemmCfg<PAIR>;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -322,6 +329,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     m0 = mb * Cfg::kTileM + (int)rank * kBM;  // this CTA's first row
     n0 = nb * kBN;
   };
+  // causal structure of the batched attention products (see above); decided per
+  // tile from the tile's row range, identically in every role and in both CTAs
+  auto tile_rows = [&](int m0) { return m0 - (int)rank * kBM; };  // first row of the whole tile
+  auto skip_tile = [&](int m0, int n0) {
+    return causal == kCausalSkipUpper && n0 >= tile_rows(m0) + Cfg::kTileM;
+  };
+  auto kb_range = [&](int m0, int& kb0, int& kb1) {
+    kb0 = 0;
+    kb1 = num_kb;
+    if (causal == kCausalKUpTo) {
+      const int k_end = min(K, tile_rows(m0) + Cfg::kTileM);
+      kb1 = (k_end + kBK - 1) / kBK;
+    } else if (causal == kCausalKFrom) {
+      kb0 = tile_rows(m0) / kBK;
+    }
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -338,8 +361,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int tile = unit; tile < tile_end && ok; tile += num_units) {
         int m0, n0, hb, sb;
         tile_origin(tile, m0, n0, hb, sb);
+        if (skip_tile(m0, n0)) continue;
+        int kb0, kb1;
+        kb_range(m0, kb0, kb1);
         const int b_n0 = n0 + (PAIR ? (int)rank * Cfg::kBLoadN : 0);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
             record_status(status, kStatusTimeout, 1);
             ok = false;
@@ -448,13 +474,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       for (int tile = unit; tile < tile_end && ok; tile += num_units) {
+        int m0, n0, hb, sb;
+        tile_origin(tile, m0, n0, hb, sb);
+        if (skip_tile(m0, n0)) continue;
+        int kb0, kb1;
+        kb_range(m0, kb0, kb1);
         if (!(PAIR ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1) : mbar_wait(&acc_empty[acc], acc_phase ^ 1))) {
           record_status(status, kStatusTimeout, 3);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!(PAIR ? mbar_wait_cluster(&full[stage], phase) : mbar_wait(&full[stage], phase))) {
             record_status(status, kStatusTimeout, 4);
             ok = false;
@@ -469,10 +500,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                         : make_sdesc_sw128(a_base + kk * 32, 16, 1024);
             const uint64_t bdesc = B_MN ? make_sdesc_sw128(b_base + kk * 2048, kChunkBytes, 1024)
                                         : make_sdesc_sw128(b_base + kk * 32, 16, 1024);
+            const uint32_t accumulate = (kb != kb0 || kk != 0) ? 1u : 0u;
             if constexpr (PAIR)
-              umma_bf16_pair(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
             else
-              umma_bf16(d_tmem, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
           }
           // the smem stage (of both CTAs) is free once these MMAs have read it
           if constexpr (PAIR)
@@ -512,6 +544,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int tile = unit; tile < tile_end; tile += num_units) {
       int m0, n0, hb, sb;
       tile_origin(tile, m0, n0, hb, sb);
+      if (skip_tile(m0, n0)) continue;
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
