@@ -192,6 +192,47 @@ def workload_config(wl, slice_mode, world):
                   % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9)}
 
 
+def other_workloads(dev, stream, steps=5, warmup=2):
+    """fwd+bwd TFLOP/s of the smaller named workloads, each step being all of its
+    micro-batches (the first writes the gradients, the rest add).  The sweep runs
+    one slice per call, as its workload description says; the others all slices
+    per call."""
+    import torch
+    from transformer_lm_megatron_gb300 import inputs as gin
+    from transformer_lm_megatron_gb300 import mlp
+    out = {}
+    for name in ("tiny", "small", "mid", "sweep1", "sweep4", "sweep16", "sweep32"):
+        w = gin.WORKLOADS[name]
+        mode = "each" if name.startswith("sweep") else "all"
+        weights = gin.make_weights(w.h, w.ffn, device=dev)
+        mbs = [gin.make_microbatch(w.tokens, w.h, j, device=dev) for j in range(min(w.k, 4))]
+        buf = mlp.BlockBuffers(w.tokens, w.h, w.ffn, w.t, device=dev)
+
+        def step():
+            for j in range(w.k):
+                X, dO = mbs[j % len(mbs)]
+                mlp.block_step(w, weights, X, dO, buf, token_offset=j * w.tokens, slice_mode=mode, stream=stream,
+                               accumulate=j > 0)
+
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / steps
+        out[name] = {"tokens": w.tokens, "h": w.h, "ffn": w.ffn, "t": w.t, "micro_batches": w.k,
+                     "slice_calls": mode, "ms_per_step": ms, "TFLOPs": w.flops_total() / (ms / 1e3) / 1e12}
+        del weights, mbs, buf
+    if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
+        raise RuntimeError(mlp.last_error())
+    return out
+
+
 ATTN_SHAPE = dict(h=20480, nh=128, t=8, seq_len=2048, tokens=2048)
 
 
@@ -491,6 +532,11 @@ def run_ours(args, wl, rank, world, dist):
                 "hyper": {k: v for k, v in hp.items()}}
         del masters, ms_state, vs_state
 
+    # ---- the other named workloads (secondary figures; the headline is the MT-NLG layer)
+    others = None
+    if not args.no_others and wl.name == "mtnlg":
+        others = other_workloads(dev, stream)
+
     # ---- next row: the tensor-sliced self-attention block at the MT-NLG layer
     # shape (h 20480, 128 heads, t 8, one 2048-token sequence), forward + backward
     attn = None
@@ -549,6 +595,7 @@ def run_ours(args, wl, rank, world, dist):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clock_info,
+        "other_workloads": others,
         "next_rows": {"adam_step": adam, "attn_block": attn},
     }
     print(json.dumps(line), flush=True)
@@ -568,6 +615,7 @@ def main():
     ap.add_argument("--no-trace", dest="trace", action="store_false")
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention-block measurement")
+    ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--reset-each-step", action="store_true",
                     help="time grad_accum_reset + all micro-batches adding, instead of the first writing")
     args = ap.parse_args()

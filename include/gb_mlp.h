@@ -228,6 +228,16 @@ int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream);
  */
 int mlp_set_cta_pair(int mode);
 
+/*
+ * mlp_set_dependent_launch - enable (1, the default) or disable (0), for later
+ * calls in this process, programmatic dependent launch: each kernel may be
+ * scheduled while the previous kernel on its stream finishes, so its prologue
+ * overlaps that kernel's tail; every kernel waits for the previous kernel's
+ * results before it touches global memory, so results do not change.
+ * Returns MLP_OK or MLP_EINVAL.
+ */
+int mlp_set_dependent_launch(int enable);
+
 /* mlp_launch_count - number of kernels this library has launched in this process. */
 uint64_t mlp_launch_count(void);
 

@@ -191,6 +191,27 @@ def test_bounded_wait_reports_timeout():
     assert float(x.sum()) == 16.0
 
 
+def test_trace_reports_every_launch_in_order():
+    s = Shape(tokens=256, h=128, ffn=512, t=2, k=1)
+    w_dev, mbs_dev, _, _ = make_case(s)
+    buf = mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t)
+    tr = mlp.Trace(capacity=64)
+    tr.start()
+    mlp.block_step(s, w_dev, *mbs_dev[0], buf, accumulate=False)
+    torch.cuda.synchronize()
+    entries = tr.stop()
+    kinds = [k for k, _, _ in entries]
+    # forward F1, F2; backward B1, B2, da column sum, B5, B3, B4
+    assert kinds == [0, 1, 10, 2, 11, 5, 3, 4]
+    mnk = [m for _, m, _ in entries]
+    assert mnk[0] == (s.tokens, s.ffn, s.h) and mnk[3] == (s.tokens, s.ffn, s.h)
+    assert mnk[5] == (s.tokens, s.h, s.ffn)
+    assert mnk[6] == (s.ffn, s.h, s.tokens) and mnk[7] == (s.h, s.ffn, s.tokens)
+    assert all(t_ms > 0 for _, _, t_ms in entries)
+    with pytest.raises(mlp.MLPError):
+        tr.stop()                                    # no trace running
+
+
 def test_launch_counter_counts_kernels():
     s = Shape(tokens=128, h=64, ffn=256, t=2, k=1)
     w_dev, mbs_dev, _, _ = make_case(s)
@@ -205,3 +226,24 @@ def test_launch_counter_counts_kernels():
     torch.cuda.synchronize()
     # one call per slice: 2 GEMMs per slice forward; 1 + 5 per slice backward
     assert mlp.mlp_launch_count() - n1 == 2 * s.t + 1 + 5 * s.t
+
+
+@pytest.mark.parametrize("mode", ["all", "each"])
+def test_dependent_launch_changes_no_bit(mode):
+    """Programmatic dependent launch only lets a kernel's prologue overlap the
+    previous kernel: outputs and gradients are bit-identical with it on and off.
+    Both call modes are deterministic: no atomics, fixed-order column sums, and
+    each fp32 reduction in HBM adds one tile per launch, launches in slice order."""
+    s = Shape(tokens=1000, h=384, ffn=1536, t=4, k=3)
+    w_dev, mbs_dev, _, _ = make_case(s)
+    try:
+        mlp.mlp_set_dependent_launch(False)
+        o_off, g_off = run_gpu(s, w_dev, mbs_dev, slice_mode=mode)
+        mlp.mlp_set_dependent_launch(True)
+        o_on, g_on = run_gpu(s, w_dev, mbs_dev, slice_mode=mode)
+    finally:
+        mlp.mlp_set_dependent_launch(True)
+    for k in o_off[-1]:
+        assert torch.equal(o_on[-1][k], o_off[-1][k]), k
+    for k in g_off:
+        assert torch.equal(g_on[k], g_off[k]), k

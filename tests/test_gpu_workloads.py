@@ -131,7 +131,8 @@ def test_mtnlg_layer_one_slice_calls_sampled_parity():
     _sampled_check(gin.WORKLOADS["mtnlg"], "each", n_rows=8, n_entries=32, seed=1)
 
 
-@pytest.mark.parametrize("name,first_overwrites", [("sweep4", False), ("sweep16", True)])
+@pytest.mark.parametrize("name,first_overwrites", [("sweep1", True), ("sweep4", False), ("sweep16", True),
+                                                   ("sweep32", False)])
 def test_accumulation_sweep_sampled_parity(name, first_overwrites):
     """h 8192, ffn 32768, t 4, one slice per call in turn, micro-batches accumulated."""
     _sampled_check(gin.WORKLOADS[name], "each", n_rows=12, n_entries=48, first_overwrites=first_overwrites)

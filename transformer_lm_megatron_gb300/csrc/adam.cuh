@@ -34,6 +34,8 @@ __device__ __forceinline__ void adam_one(const AdamParams& p, float g, float& w,
 __global__ void __launch_bounds__(256) k_adam_step(int64_t n, const float* __restrict__ grad, float* __restrict__ w,
                                                    float* __restrict__ m, float* __restrict__ v,
                                                    uint16_t* __restrict__ w16, AdamParams p) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t n4 = n >> 2;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += stride) {

@@ -48,6 +48,8 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* red) {
 __global__ void __launch_bounds__(kSoftmaxThreads)
     k_softmax_rows(const float* __restrict__ S, uint16_t* __restrict__ P, int64_t rows, int cols) {
   __shared__ float red[kSoftmaxThreads / 32];
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const float* s = S + r * cols;
     uint16_t* p = P + r * cols;
@@ -89,6 +91,8 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
     k_softmax_bwd_rows(const uint16_t* __restrict__ P, const float* __restrict__ dP, uint16_t* __restrict__ dS,
                        int64_t rows, int cols, float alpha) {
   __shared__ float red[kSoftmaxThreads / 32];
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const uint16_t* p = P + r * cols;
     const float* g = dP + r * cols;

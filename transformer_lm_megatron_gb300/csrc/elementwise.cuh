@@ -4,10 +4,11 @@
 //   (+)= adds to the accumulator, or overwrites it for the first micro-batch of a step
 //   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
 //
-// Column sums are deterministic: one CTA owns 64 columns for every row, each of
-// its 64 row-lanes sums a fixed row subset, and the 64 partial sums are added in
-// a fixed order.  Loads and stores are 16-byte vectors; a warp covers four
-// 128-byte row segments per instruction.
+// Column sums are deterministic: a cluster of 8 CTAs owns 64 columns, each CTA
+// a fixed eighth of the rows; each of a CTA's 64 row-lanes sums a fixed row
+// subset, the lanes' sums are added in a fixed order, and CTA 0 adds the 8 CTAs'
+// sums in rank order through distributed shared memory.  Loads and stores are
+// 16-byte vectors; a warp covers four 128-byte row segments per instruction.
 #pragma once
 #include <cstdint>
 
@@ -19,102 +20,113 @@ namespace gbmlp {
 constexpr int kColRowLanes = 64;                 // threads along the rows of a column strip
 constexpr int kColThreads = 8 * kColRowLanes;    // 8 column groups (8 bf16 = 16 B each) x row lanes
 constexpr int kColsPerCta = 64;
+constexpr int kColRowSplit = 8;                  // CTAs of a cluster, each summing 1/8 of the rows
 
-// Fixed-order sum of the row lanes' partial column sums; part is [kColRowLanes][kColsPerCta + 1].
-__device__ __forceinline__ float colsum_reduce(float (*part)[kColsPerCta + 1], int col_in_cta) {
+// Deterministic column sums over a cluster of kColRowSplit CTAs (grid y = rank):
+// every CTA reduces its row range to 64 partial sums in a fixed order, then CTA 0
+// adds the 8 partial vectors, in rank order, through distributed shared memory.
+// part is [kColRowLanes][kColsPerCta + 1]; returns the total for thread
+// threadIdx.x < kColsPerCta of CTA rank 0 (0 elsewhere).
+__device__ __forceinline__ float cluster_colsum(float (*part)[kColsPerCta + 1], float* psum) {
+  if (threadIdx.x < kColsPerCta) {
+    float tot = 0.0f;
+    for (int k = 0; k < kColRowLanes; ++k) tot += part[k][threadIdx.x];
+    psum[threadIdx.x] = tot;
+  }
+  cluster_sync();  // every CTA's partial vector is complete
   float tot = 0.0f;
-  for (int k = 0; k < kColRowLanes; ++k) tot += part[k][col_in_cta];
+  if (cluster_ctarank() == 0 && threadIdx.x < kColsPerCta) {
+    for (unsigned r = 0; r < kColRowSplit; ++r) {
+      const float* peer = static_cast<const float*>(__cluster_map_shared_rank(static_cast<void*>(psum), r));
+      tot += peer[threadIdx.x];
+    }
+  }
+  cluster_sync();  // the peers' shared memory stays alive until CTA 0 has read it
   return tot;
 }
 
 // dZ = dO * keep * scale (rounded to bf16); db[c] (+)= sum over rows of the rounded dZ.
-// Each thread handles two rows per iteration so that two 16-byte loads are in flight.
+// Grid (ceil(cols / 64), kColRowSplit), clusters of (1, kColRowSplit, 1).
 __global__ void __launch_bounds__(kColThreads)
     k_dropout_bwd_colsum(const uint16_t* __restrict__ dO, uint16_t* __restrict__ dZ, float* __restrict__ db,
                          int64_t rows, int cols, DropoutParams drop, int accumulate) {
   __shared__ float part[kColRowLanes][kColsPerCta + 1];
+  __shared__ float psum[kColsPerCta];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
   const int col = blockIdx.x * kColsPerCta + cg * 8;
+  const int64_t r_begin = rows * (int64_t)blockIdx.y / kColRowSplit;
+  const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / kColRowSplit;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (col < cols) {
-    for (int64_t r0 = rl; r0 < rows; r0 += 2 * kColRowLanes) {
-      const int64_t r1 = r0 + kColRowLanes;
-      const bool two = r1 < rows;
-      const uint4 q0 = *reinterpret_cast<const uint4*>(dO + r0 * cols + col);
-      const uint4 q1 = two ? *reinterpret_cast<const uint4*>(dO + r1 * cols + col) : make_uint4(0, 0, 0, 0);
+    for (int64_t r = r_begin + rl; r < r_end; r += kColRowLanes) {
+      const int64_t off = r * cols + col;
+      const uint4 q = *reinterpret_cast<const uint4*>(dO + off);
+      float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
+                    bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
+      const uint32_t keep = dropout_keep8(drop, r, col);
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if (half == 1 && !two) break;
-        const uint4 q = half ? q1 : q0;
-        const int64_t r = half ? r1 : r0;
-        float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
-                      bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
-        const uint32_t keep = dropout_keep8(drop, r, col);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          v[j] = round_bf16_f(((keep >> j) & 1u) ? v[j] * drop.scale : 0.0f);
-          s[j] += v[j];
-        }
-        uint4 o;
-        o.x = pack_bf16x2(v[0], v[1]);
-        o.y = pack_bf16x2(v[2], v[3]);
-        o.z = pack_bf16x2(v[4], v[5]);
-        o.w = pack_bf16x2(v[6], v[7]);
-        *reinterpret_cast<uint4*>(dZ + r * cols + col) = o;
+      for (int j = 0; j < 8; ++j) {
+        v[j] = round_bf16_f(((keep >> j) & 1u) ? v[j] * drop.scale : 0.0f);
+        s[j] += v[j];
       }
+      uint4 o;
+      o.x = pack_bf16x2(v[0], v[1]);
+      o.y = pack_bf16x2(v[2], v[3]);
+      o.z = pack_bf16x2(v[4], v[5]);
+      o.w = pack_bf16x2(v[6], v[7]);
+      *reinterpret_cast<uint4*>(dZ + off) = o;
     }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[rl][cg * 8 + j] = s[j];
   __syncthreads();
-  if (threadIdx.x < kColsPerCta) {
+  const float tot = cluster_colsum(part, psum);
+  if (blockIdx.y == 0 && threadIdx.x < kColsPerCta) {
     const int c = blockIdx.x * kColsPerCta + threadIdx.x;
-    if (c < cols) {
-      const float tot = colsum_reduce(part, threadIdx.x);
-      db[c] = accumulate ? db[c] + tot : tot;
-    }
+    if (c < cols) db[c] = accumulate ? db[c] + tot : tot;
   }
 }
 
-// out[c] (+)= sum over rows of x[r * ld + c], c < cols.
+// out[c] (+)= sum over rows of x[r * ld + c], c < cols.  Same grid and clusters.
 __global__ void __launch_bounds__(kColThreads)
     k_colsum_bf16(const uint16_t* __restrict__ x, int64_t ld, float* __restrict__ out, int64_t rows, int cols,
                   int accumulate) {
   __shared__ float part[kColRowLanes][kColsPerCta + 1];
+  __shared__ float psum[kColsPerCta];
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
   const int col = blockIdx.x * kColsPerCta + cg * 8;
+  const int64_t r_begin = rows * (int64_t)blockIdx.y / kColRowSplit;
+  const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / kColRowSplit;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (col < cols) {
-    for (int64_t r0 = rl; r0 < rows; r0 += 2 * kColRowLanes) {
-      const int64_t r1 = r0 + kColRowLanes;
-      const uint4 q0 = *reinterpret_cast<const uint4*>(x + r0 * ld + col);
-      const uint4 q1 = r1 < rows ? *reinterpret_cast<const uint4*>(x + r1 * ld + col) : make_uint4(0, 0, 0, 0);
-      s[0] += bf16lo(q0.x); s[1] += bf16hi(q0.x);
-      s[2] += bf16lo(q0.y); s[3] += bf16hi(q0.y);
-      s[4] += bf16lo(q0.z); s[5] += bf16hi(q0.z);
-      s[6] += bf16lo(q0.w); s[7] += bf16hi(q0.w);
-      s[0] += bf16lo(q1.x); s[1] += bf16hi(q1.x);
-      s[2] += bf16lo(q1.y); s[3] += bf16hi(q1.y);
-      s[4] += bf16lo(q1.z); s[5] += bf16hi(q1.z);
-      s[6] += bf16lo(q1.w); s[7] += bf16hi(q1.w);
+    for (int64_t r = r_begin + rl; r < r_end; r += kColRowLanes) {
+      const uint4 q = *reinterpret_cast<const uint4*>(x + r * ld + col);
+      s[0] += bf16lo(q.x); s[1] += bf16hi(q.x);
+      s[2] += bf16lo(q.y); s[3] += bf16hi(q.y);
+      s[4] += bf16lo(q.z); s[5] += bf16hi(q.z);
+      s[6] += bf16lo(q.w); s[7] += bf16hi(q.w);
     }
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[rl][cg * 8 + j] = s[j];
   __syncthreads();
-  if (threadIdx.x < kColsPerCta) {
+  const float tot = cluster_colsum(part, psum);
+  if (blockIdx.y == 0 && threadIdx.x < kColsPerCta) {
     const int c = blockIdx.x * kColsPerCta + threadIdx.x;
-    if (c < cols) {
-      const float tot = colsum_reduce(part, threadIdx.x);
-      out[c] = accumulate ? out[c] + tot : tot;
-    }
+    if (c < cols) out[c] = accumulate ? out[c] + tot : tot;
   }
 }
 
 // p[0 .. n) = 0 with 16-byte stores; n % 4 == 0 and p 16-byte aligned.
 __global__ void k_zero_f32(float* __restrict__ p, int64_t n) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t n4 = n / 4;
   float4* p4 = reinterpret_cast<float4*>(p);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
@@ -124,6 +136,8 @@ __global__ void k_zero_f32(float* __restrict__ p, int64_t n) {
 // m[r * cols + c] = keep(r, c) ? 1 : 0, eight columns per thread with the same
 // routine the block's kernels use (cols % 8 == 0), else one element per thread.
 __global__ void k_dropout_mask(uint8_t* __restrict__ m, int64_t rows, int cols, DropoutParams drop) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   if (cols % 8 == 0) {
     const int64_t n8 = rows * (int64_t)(cols / 8);
@@ -145,6 +159,8 @@ __global__ void k_dropout_mask(uint8_t* __restrict__ m, int64_t rows, int cols, 
 
 // y = GeLU(x), dy = GeLU'(x) with the epilogues' device functions.
 __global__ void k_gelu_probe(const float* __restrict__ x, int64_t n, float* __restrict__ y, float* __restrict__ dy) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     y[i] = gelu_f(x[i]);
     dy[i] = gelu_prime_f(x[i]);
@@ -155,6 +171,8 @@ __global__ void k_gelu_probe(const float* __restrict__ x, int64_t n, float* __re
 // a timeout in the status word: exercises the bounded-wait error path.
 __global__ void k_wait_timeout_probe(int* status, uint64_t limit_ns) {
   __shared__ uint64_t bar;
+  grid_dependency_wait();
+  grid_launch_dependents();
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();

@@ -20,6 +20,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -143,6 +144,41 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Programmatic dependent launch: a kernel may be scheduled while the previous
+// kernel on its stream drains, running its prologue (barriers, TMEM, descriptor
+// prefetch) early; every kernel of this library executes griddepcontrol.wait
+// before its first global-memory access, so results are unchanged.  On by default.
+std::atomic<int> g_pdl{1};
+
+// Launch through cudaLaunchKernelEx with an optional (cx, cy, 1) cluster and the
+// programmatic-serialization attribute.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, unsigned cx,
+                          unsigned cy, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (cx * cy > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cx;
+    attr[n].val.clusterDim.y = cy;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (g_pdl.load(std::memory_order_relaxed)) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 #include "gemm_host.cuh"
 
 DropoutParams make_dropout(float p, uint64_t seed, uint64_t token_offset, int h) {
@@ -175,9 +211,9 @@ int check_ptrs(const char* what, std::initializer_list<const void*> ptrs) {
   return MLP_OK;
 }
 
-int launch_check(const char* what) {
+int launch_check(cudaError_t e, const char* what) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLP_ECUDA, "%s launch: %s", what, cudaGetErrorString(e));
   return MLP_OK;
 }
@@ -274,10 +310,11 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   if (first_call) {
     // B1: dZ = dO * m / (1 - p), db += sum_tok dZ
     const int ts = trace_pre(s);
-    k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dO, dZ, db, tokens, h, drop,
-                                                                                      accumulate ? 1 : 0);
+    const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, kColRowSplit),
+                                        dim3(kColThreads), 0, s, 1, kColRowSplit, dO, dZ, db, tokens, h, drop,
+                                        accumulate ? 1 : 0);
     trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
-    rc = launch_check("dropout backward");
+    rc = launch_check(e, "dropout backward");
     if (rc) return rc;
   }
   const int i0 = slice < 0 ? 0 : slice;
@@ -294,25 +331,15 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     if (rc) return rc;
     // da_i += sum_tok dU_i
     const int ts = trace_pre(s);
-    k_colsum_bf16<<<(f + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dU + c, ffn, da + c, tokens, f,
-                                                                               accumulate ? 1 : 0);
+    const cudaError_t e = launch_kernel(k_colsum_bf16, dim3((f + kColsPerCta - 1) / kColsPerCta, kColRowSplit),
+                                        dim3(kColThreads), 0, s, 1, kColRowSplit, (const uint16_t*)(dU + c),
+                                        (int64_t)ffn, da + c, tokens, f, accumulate ? 1 : 0);
     trace_post(ts, s, kTraceColsum, tokens, f, 0);
-    rc = launch_check("bias-gradient column sum");
+    rc = launch_check(e, "bias-gradient column sum");
     if (rc) return rc;
-    // B3: dB_i (+)= Y_i^T dZ                             (M = f, N = h, K = T)
-    EpiParams e3{};
-    e3.kind = accumulate ? kEpiF32Add : kEpiF32Store;
-    e3.ld = h;
-    e3.g_out = dB + c * h;
-    rc = gemm(st, Y + c, true, ffn, dZ, true, h, f, h, T, e3, s, kTraceB3);
-    if (rc) return rc;
-    // B4: dA_i (+)= X^T dU_i                             (M = h, N = f, K = T)
-    EpiParams e4{};
-    e4.kind = accumulate ? kEpiF32Add : kEpiF32Store;
-    e4.ld = ffn;
-    e4.g_out = dA + c;
-    rc = gemm(st, X, true, h, dU + c, true, ffn, h, f, T, e4, s, kTraceB4);
-    if (rc) return rc;
+    // B5, B3 and B4 read only dU (B2), dZ (B1) and the forward's tensors, so each
+    // may start while its predecessor drains (late dependency wait); B5 goes
+    // first, so that B3's tiles fill B5's last, partial wave.
     // B5: dX (+)= dU_i A_i^T; the last slice adds dO and writes bf16   (M = T, N = h, K = f)
     EpiParams e5{};
     e5.ld = h;
@@ -325,7 +352,21 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
       e5.kind = (i == 0) ? kEpiF32Store : kEpiF32Add;
       e5.g_out = dXacc;
     }
-    rc = gemm(st, dU + c, false, ffn, A + c, false, ffn, T, h, f, e5, s, kTraceB5);
+    rc = gemm(st, dU + c, false, ffn, A + c, false, ffn, T, h, f, e5, s, kTraceB5, true);
+    if (rc) return rc;
+    // B3: dB_i (+)= Y_i^T dZ                             (M = f, N = h, K = T)
+    EpiParams e3{};
+    e3.kind = accumulate ? kEpiF32Add : kEpiF32Store;
+    e3.ld = h;
+    e3.g_out = dB + c * h;
+    rc = gemm(st, Y + c, true, ffn, dZ, true, h, f, h, T, e3, s, kTraceB3, true);
+    if (rc) return rc;
+    // B4: dA_i (+)= X^T dU_i                             (M = h, N = f, K = T)
+    EpiParams e4{};
+    e4.kind = accumulate ? kEpiF32Add : kEpiF32Store;
+    e4.ld = ffn;
+    e4.g_out = dA + c;
+    rc = gemm(st, X, true, h, dU + c, true, ffn, h, f, T, e4, s, kTraceB4, true);
     if (rc) return rc;
   }
   return MLP_OK;
@@ -348,9 +389,9 @@ int grad_accum_reset(int h, int ffn, float* dA, float* da, float* dB, float* db,
     if (blocks > (int64_t)st->sms * 8) blocks = (int64_t)st->sms * 8;
     if (blocks < 1) blocks = 1;
     const int ts = trace_pre(s);
-    k_zero_f32<<<(int)blocks, 256, 0, s>>>(bufs[k], sizes[k]);
+    const cudaError_t e = launch_kernel(k_zero_f32, dim3((unsigned)blocks), dim3(256), 0, s, 1, 1, bufs[k], sizes[k]);
     trace_post(ts, s, kTraceZero, sizes[k], 0, 0);
-    rc = launch_check("grad_accum_reset");
+    rc = launch_check(e, "grad_accum_reset");
     if (rc) return rc;
   }
   return MLP_OK;
@@ -372,12 +413,13 @@ int softmax_launch(DeviceState* st, bool backward, const uint16_t* P_in, const f
                    int cols, float alpha, cudaStream_t s) {
   int64_t blocks = rows < (int64_t)st->sms * 16 ? rows : (int64_t)st->sms * 16;
   const int ts = trace_pre(s);
-  if (backward)
-    k_softmax_bwd_rows<<<(int)blocks, kSoftmaxThreads, 0, s>>>(P_in, F_in, out, rows, cols, alpha);
-  else
-    k_softmax_rows<<<(int)blocks, kSoftmaxThreads, 0, s>>>(F_in, out, rows, cols);
+  const cudaError_t e =
+      backward ? launch_kernel(k_softmax_bwd_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, P_in,
+                               F_in, out, rows, cols, alpha)
+               : launch_kernel(k_softmax_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, F_in, out,
+                               rows, cols);
   trace_post(ts, s, kTraceSoftmax, rows, cols, 0);
-  return launch_check(backward ? "softmax backward" : "softmax");
+  return launch_check(e, backward ? "softmax backward" : "softmax");
 }
 
 int adam_step(int64_t n, const float* grad, float grad_scale, float* master, float* m, float* v, mlp_bf16* weight,
@@ -412,9 +454,10 @@ int adam_step(int64_t n, const float* grad, float grad_scale, float* master, flo
   if (blocks > (int64_t)st->sms * 8) blocks = (int64_t)st->sms * 8;
   if (blocks < 1) blocks = 1;
   const int ts = trace_pre(s);
-  k_adam_step<<<(int)blocks, 256, 0, s>>>(n, grad, master, m, v, weight, p);
+  const cudaError_t e =
+      launch_kernel(k_adam_step, dim3((unsigned)blocks), dim3(256), 0, s, 1, 1, n, grad, master, m, v, weight, p);
   trace_post(ts, s, kTraceAdam, n, 0, 0);
-  return launch_check("adam_step");
+  return launch_check(e, "adam_step");
 }
 
 int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
@@ -486,10 +529,10 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   {
     const DropoutParams drop = make_dropout(p, seed, token_offset, h);
     const int ts = trace_pre(s);
-    k_dropout_bwd_colsum<<<(h + kColsPerCta - 1) / kColsPerCta, kColThreads, 0, s>>>(dOut, dZ, dbo, tokens, h, drop,
-                                                                                      acc);
+    const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, kColRowSplit),
+                                        dim3(kColThreads), 0, s, 1, kColRowSplit, dOut, dZ, dbo, tokens, h, drop, acc);
     trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
-    rc = launch_check("dropout backward");
+    rc = launch_check(e, "dropout backward");
     if (rc) return rc;
   }
   // dWo (+)= O^T dZ
@@ -528,10 +571,12 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   // dbqkv (+)= sum dQKV; dWqkv (+)= X^T dQKV; dX = [dOut +] dQKV Wqkv^T
   {
     const int ts = trace_pre(s);
-    k_colsum_bf16<<<(int)((h3 + kColsPerCta - 1) / kColsPerCta), kColThreads, 0, s>>>(dQKV, h3, dbqkv, tokens,
-                                                                                       (int)h3, acc);
+    const cudaError_t e =
+        launch_kernel(k_colsum_bf16, dim3((unsigned)((h3 + kColsPerCta - 1) / kColsPerCta), kColRowSplit),
+                      dim3(kColThreads), 0, s, 1, kColRowSplit, (const uint16_t*)dQKV, (int64_t)h3, dbqkv, tokens,
+                      (int)h3, acc);
     trace_post(ts, s, kTraceColsum, tokens, h3, 0);
-    rc = launch_check("bias-gradient column sum");
+    rc = launch_check(e, "bias-gradient column sum");
     if (rc) return rc;
   }
   EpiParams eq{};
@@ -576,8 +621,9 @@ int mlp_dropout_mask(int h, int64_t tokens, float p, uint64_t seed, uint64_t tok
   int rc = device_state(&st);
   if (rc) return rc;
   const DropoutParams drop = make_dropout(p, seed, token_offset, h);
-  k_dropout_mask<<<st->sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(m, tokens, h, drop);
-  return launch_check("dropout mask");
+  const cudaError_t e = launch_kernel(k_dropout_mask, dim3(st->sms * 4), dim3(256), 0,
+                                      static_cast<cudaStream_t>(stream), 1, 1, m, tokens, h, drop);
+  return launch_check(e, "dropout mask");
 }
 
 int mlp_gelu_probe(const float* x, int64_t n, float* y, float* dy, void* stream) {
@@ -585,8 +631,9 @@ int mlp_gelu_probe(const float* x, int64_t n, float* y, float* dy, void* stream)
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;
-  k_gelu_probe<<<st->sms * 4, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, n, y, dy);
-  return launch_check("gelu probe");
+  const cudaError_t e =
+      launch_kernel(k_gelu_probe, dim3(st->sms * 4), dim3(256), 0, static_cast<cudaStream_t>(stream), 1, 1, x, n, y, dy);
+  return launch_check(e, "gelu probe");
 }
 
 int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream) {
@@ -594,8 +641,9 @@ int mlp_wait_timeout_probe(uint64_t limit_ns, void* stream) {
   DeviceState* st = nullptr;
   int rc = device_state(&st);
   if (rc) return rc;
-  k_wait_timeout_probe<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(st->status, limit_ns);
-  return launch_check("wait-timeout probe");
+  const cudaError_t e = launch_kernel(k_wait_timeout_probe, dim3(1), dim3(32), 0, static_cast<cudaStream_t>(stream),
+                                      1, 1, st->status, limit_ns);
+  return launch_check(e, "wait-timeout probe");
 }
 
 uint64_t mlp_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
@@ -603,6 +651,12 @@ uint64_t mlp_launch_count(void) { return g_launches.load(std::memory_order_relax
 int mlp_set_cta_pair(int mode) {
   if (mode < -1 || mode > 1) return fail(MLP_EINVAL, "mlp_set_cta_pair: mode %d not in {-1, 0, 1}", mode);
   g_pair_mode.store(mode, std::memory_order_relaxed);
+  return MLP_OK;
+}
+
+int mlp_set_dependent_launch(int enable) {
+  if (enable != 0 && enable != 1) return fail(MLP_EINVAL, "mlp_set_dependent_launch: %d not in {0, 1}", enable);
+  g_pdl.store(enable, std::memory_order_relaxed);
   return MLP_OK;
 }
 

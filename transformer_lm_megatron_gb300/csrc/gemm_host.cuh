@@ -1,7 +1,8 @@
 // Host side of the tcgen05 GEMM: TMA descriptors of the operands and outputs,
 // the choice of variant (single CTA or CTA pair), tile order and L2 policy, and the
 // launch.  Included by gb_mlp.cu inside its anonymous namespace; it uses that
-// file's DeviceState, fail(), g_encode, g_launches and trace_pre()/trace_post().
+// file's DeviceState, fail(), g_encode, g_launches, launch_kernel() and
+// trace_pre()/trace_post().
 #pragma once
 
 // L2 policies of the GEMMs' TMA copies (see k_gemm_bf16_tc): none by default.
@@ -12,6 +13,19 @@ constexpr int64_t kGroupBytes = 32ll << 20;
 
 // -1: CTA pairs whenever a tile has more than 128 rows; 0: single CTAs; 1: CTA pairs.
 std::atomic<int> g_pair_mode{-1};
+
+// Scheduling choices that change no result, kept switchable to measure them:
+// paced epilogue stores, and late dependency waits of mlp_bwd's last GEMMs.
+std::atomic<int> g_epi_pace{1};
+std::atomic<int> g_late_wait{1};
+
+// Late dependency waits pay only for short GEMMs: there the next launch's tiles
+// fill the partial last wave and the pipeline drain of the one before.  Tiles are
+// dealt to CTAs statically, so on a GEMM of many waves the CTAs that started early
+// only finish early, and the idle time moves to the end of the chain instead of
+// going away (measured: slightly slower on the 6.9 TFLOP GEMMs of the MT-NLG
+// layer, faster on GEMMs of 0.3 TFLOP and below).
+constexpr double kLateWaitMaxFlop = 5.5e11;
 
 // 2-D bf16 tensor map: `inner` contiguous elements per row, `outer` rows, row
 // pitch `ld` elements; box {box_inner, box_outer}; 128-byte swizzle; out-of-range
@@ -75,7 +89,7 @@ template <bool AM, bool BM, bool PAIR, bool BATCHED = false>
 int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                   const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
                   int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind, int batch = 1,
-                  int nb_h = 1, int causal = kCausalNone) {
+                  int nb_h = 1, int causal = kCausalNone, bool late_wait = false) {
   using Cfg = GemmCfg<PAIR>;
   auto kern = k_gemm_bf16_tc<AM, BM, PAIR, BATCHED>;
   const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0) + (BATCHED ? 8 : 0);
@@ -106,29 +120,22 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
     st->gemm_attr[slot] = true;
   }
   const int64_t tiles = (int64_t)((M + Cfg::kTileM - 1) / Cfg::kTileM) * ((N + kBN - 1) / kBN) * batch;
+  EpiParams epx = ep;
+  epx.pace = g_epi_pace.load(std::memory_order_relaxed);
+  late_wait = late_wait && g_late_wait.load(std::memory_order_relaxed) &&
+              2.0 * (double)M * (double)N * (double)K * (double)batch <= kLateWaitMaxFlop;
   const int ts = trace_pre(stream);
   cudaError_t e;
   if (PAIR) {
     const int pairs = (int)(tiles < st->max_pairs[slot] ? tiles : st->max_pairs[slot]);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (unsigned)pairs, 1, 1);
-    cfg.blockDim = dim3(kGemmThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group, l2_hints, batch,
-                           nb_h, causal, st->status);
+    e = launch_kernel(kern, dim3(2 * (unsigned)pairs), dim3(kGemmThreads), Cfg::kSmemBytes, stream, 2, 1, mA, mB, mC,
+                      mO0, mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
+                      st->status);
   } else {
     const int grid = (int)(tiles < st->sms ? tiles : st->sms);
-    kern<<<grid, kGemmThreads, Cfg::kSmemBytes, stream>>>(mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                          group, l2_hints, batch, nb_h, causal, st->status);
-    e = cudaGetLastError();
+    e = launch_kernel(kern, dim3((unsigned)grid), dim3(kGemmThreads), Cfg::kSmemBytes, stream, 1, 1, mA, mB, mC, mO0,
+                      mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
+                      st->status);
   }
   trace_post(ts, stream, trace_kind, M, N, K);
   g_launches.fetch_add(1, std::memory_order_relaxed);
@@ -138,8 +145,11 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
 }
 
 // D[M, N] = A(M x K) B(K x N) with the given operand layouts and epilogue.
+// late_wait: the launch reads nothing the previous kernel on the stream writes
+// (see k_gemm_bf16_tc); only mlp_bwd's weight-gradient and input-gradient GEMMs,
+// never the first kernel of a call.
 int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, bool b_mn, int64_t ldb, int M, int N,
-         int K, const EpiParams& ep, cudaStream_t stream, int trace_kind) {
+         int K, const EpiParams& ep, cudaStream_t stream, int trace_kind, bool late_wait = false) {
   const int mode = g_pair_mode.load(std::memory_order_relaxed);
   const bool pair = mode == 1 || (mode < 0 && M > kBM);
   CUtensorMap mA, mB, mC, mO0, mO1;
@@ -179,19 +189,19 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
   const int l2_hints = g_l2_hints.load(std::memory_order_relaxed);
   if (!a_mn && b_mn)
     return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind)
+                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait)
                 : launch_gemm_t<false, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind);
+                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
   if (!a_mn && !b_mn)
     return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind)
+                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait)
                 : launch_gemm_t<false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind);
+                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
   if (a_mn && b_mn)
     return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind)
+                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait)
                 : launch_gemm_t<true, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind);
+                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 

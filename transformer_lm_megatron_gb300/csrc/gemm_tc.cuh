@@ -21,7 +21,10 @@
 //               loop of tile j+1.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lane
 //               quarter w % 4, i.e. tile rows 32*(w%4) .. +31), fused element-wise
-//               work, vectorised global stores.
+//               work, TMA stores.  The 8 column blocks of a tile leave paced
+//               against the producer's progress through the next tile: a burst
+//               of output stores (fp32 gradients above all) starves that tile's
+//               operand copies, and the tensor pipe with them.
 // Every mbarrier wait is bounded; on timeout the kernel records kStatusTimeout in
 // the status word, drains its own copies and MMAs, frees TMEM and returns.
 #pragma once
@@ -48,6 +51,8 @@ constexpr uint32_t kTmemCols = 2 * kBN;         // double-buffered accumulator
 constexpr uint32_t kOutBoxBytes = 32 * 32 * 4;
 constexpr uint32_t kOutBoxBf16Bytes = 32 * 32 * 2;
 constexpr uint32_t kOutStageBytes = 4 * 2 * kOutBoxBytes;  // 4 warps x 2 buffers
+// Longest an epilogue warp waits for the main loop before it stores anyway.
+constexpr uint64_t kPaceLimitNs = 200000;
 
 template <bool PAIR>
 struct GemmCfg {
@@ -94,6 +99,7 @@ struct EpiParams {
   const uint16_t* bias;       // bias vector indexed by output column
   float alpha;                // scale of kEpiScaleMask
   DropoutParams drop;
+  int pace;                   // 1: pace the output stores against the next tile's main loop
 };
 
 __device__ __forceinline__ void ld_bf16x8(const uint16_t* p, float (&v)[8]) {
@@ -232,7 +238,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
-                   int group, int l2_hints, int batch, int nb_h, int causal, int* status) {
+                   int group, int l2_hints, int batch, int nb_h, int causal, int late_wait, int* status) {
   using Cfg = GemmCfg<PAIR>;
   constexpr int kStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -261,8 +267,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // A pipeline that broke in an earlier launch leaves the status word set; later
   // launches then skip their work so that a failure ends quickly.
   __shared__ int s_skip;
+  // k-blocks whose copies this CTA's producer has issued, over all its tiles so far
+  __shared__ uint32_t s_kb_issued;
+  volatile uint32_t* kb_issued = &s_kb_issued;
   if (threadIdx.x == 0) {
-    s_skip = (status != nullptr && *reinterpret_cast<volatile int*>(status) != 0) ? 1 : 0;
+    s_kb_issued = 0;
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
@@ -289,6 +298,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_alloc<PAIR>(tmem_slot, kTmemCols);
     tmem_relinquish<PAIR>();
   }
+  // Everything above touches only this CTA's own resources; from here on the
+  // kernel reads what the previous kernel on the stream wrote.  With late_wait the
+  // host guarantees that this launch reads nothing the immediately preceding
+  // kernel writes and that kernel waited for its own predecessor before letting
+  // this one start, so the main loop may overlap that kernel's tail; the wait
+  // then comes before exit, so that this grid completes only after it.
+  if (!late_wait) grid_dependency_wait();
+  grid_launch_dependents();
+  if (threadIdx.x == 0) s_skip = (status != nullptr && *reinterpret_cast<volatile int*>(status) != 0) ? 1 : 0;
   tc_fence_before();
   __syncthreads();
   if constexpr (PAIR) {
@@ -355,6 +373,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t issued[kStages];
 #pragma unroll
       for (int s = 0; s < kStages; ++s) issued[s] = 0;
+      uint32_t n_issued = 0;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
@@ -444,6 +463,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
           }
           ++issued[stage];
+          *kb_issued = ++n_issued;
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1;
@@ -541,10 +561,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint64_t pol_out = l2_policy(hout);
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t kb_end = 0;  // the producer's k-block count once this tile's copies are all issued
     for (int tile = unit; tile < tile_end; tile += num_units) {
       int m0, n0, hb, sb;
       tile_origin(tile, m0, n0, hb, sb);
       if (skip_tile(m0, n0)) continue;
+      int kb0, kb1;
+      kb_range(m0, kb0, kb1);
+      kb_end += (uint32_t)max(kb1 - kb0, 0);
+      // Reduction length of this CTA's next tile, whose main loop these stores
+      // are spread over (0: no next tile, the stores go out at once).
+      uint32_t nkb_next = 0;
+      if (tile + num_units < tile_end) {
+        int m1, n1, hb1, sb1;
+        tile_origin(tile + num_units, m1, n1, hb1, sb1);
+        if (!skip_tile(m1, n1)) {
+          int a0, a1;
+          kb_range(m1, a0, a1);
+          nkb_next = (uint32_t)max(a1 - a0, 0);
+        }
+      }
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
@@ -554,6 +590,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
 #pragma unroll 1
       for (int c0 = 0; c0 < kBN; c0 += 32) {
+        if (ep.pace && nkb_next > 0 && c0 > 0) {
+          // Pace the output: column block c0 / 32 (of 8) leaves once the producer is
+          // about (3 / 32) * (c0 / 32) of the way through the next tile's copies, so
+          // the stores spread over two thirds of that main loop instead of competing
+          // with its operand copies in one burst.  The target is always reached (the
+          // next tile's copies do not depend on this epilogue); the wait is bounded
+          // all the same and only delays.
+          const uint32_t lead = min(nkb_next, (uint32_t)kStages + ((uint32_t)(c0 >> 5) * nkb_next * 3u) / 32u);
+          if (lane == 0) {
+            const uint64_t t0 = globaltimer_ns();
+            while (*kb_issued < kb_end + lead && globaltimer_ns() - t0 < kPaceLimitNs) __nanosleep(128);
+          }
+          __syncwarp();
+        }
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c0, r);
         tmem_ld_wait();
@@ -650,6 +700,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     tmem_dealloc<PAIR>(tmem_base, kTmemCols);
   }
+  if (late_wait) grid_dependency_wait();
 }
 
 }  // namespace gbmlp
