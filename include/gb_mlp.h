@@ -238,6 +238,18 @@ int mlp_set_cta_pair(int mode);
  */
 int mlp_set_dependent_launch(int enable);
 
+/*
+ * mlp_set_split_tail - enable (1, the default) or disable (0), for later calls in
+ * this process, the split tail of the GEMMs with a bf16 epilogue: when a GEMM's last
+ * wave of output tiles would occupy at most half of the CTA pairs (CTAs), each of
+ * those tiles is computed as two halves of its reduction by two pairs, whose fp32
+ * partial sums are added (in either order: the sum is the same) before the
+ * epilogue.  Results stay deterministic; they differ from the unsplit ones only by
+ * fp32 summation order.  The partial sums use 20 MB of statically allocated device
+ * memory.  Returns MLP_OK or MLP_EINVAL.
+ */
+int mlp_set_split_tail(int enable);
+
 /* mlp_launch_count - number of kernels this library has launched in this process. */
 uint64_t mlp_launch_count(void);
 

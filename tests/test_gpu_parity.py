@@ -247,3 +247,34 @@ def test_dependent_launch_changes_no_bit(mode):
         assert torch.equal(o_on[-1][k], o_off[-1][k]), k
     for k in g_off:
         assert torch.equal(g_on[k], g_off[k]), k
+
+
+@pytest.mark.parametrize("cta_pair_mode", [0, 1], indirect=True, ids=["single", "pair"])
+@pytest.mark.parametrize("tokens,h,ffn,t", [
+    (512, 1280, 2048, 1),   # every GEMM with a bf16 epilogue has fewer tiles than half the CTA pairs
+    (456, 1288, 1552, 2),   # the same with ragged M, N and K (K of F2/B5 not a multiple of 64)
+])
+def test_split_tail_full_parity(tokens, h, ffn, t, cta_pair_mode):
+    """GEMMs whose last wave is at most half full run their tail tiles as two
+    half-reductions (split tail).  These shapes put F1, F2, B2 and B5 entirely in
+    the tail: full parity with the oracle, bit-identical repeats (the two partial
+    sums commute), and agreement with the unsplit kernel to fp32 rounding."""
+    s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2, p=0.1)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    g_outs, g_grads = run_gpu(s, w_dev, mbs_dev, keep_all=True)
+    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True, keep_all=True)
+    compare_full(s, g_outs, g_grads, r_outs, r_grads, label=f"split tail, pair mode {cta_pair_mode}")
+    again_outs, again_grads = run_gpu(s, w_dev, mbs_dev, keep_all=True)
+    for j in range(s.k):
+        for k in g_outs[j]:
+            assert torch.equal(again_outs[j][k], g_outs[j][k]), (j, k)
+    try:
+        mlp.mlp_set_split_tail(False)
+        u_outs, u_grads = run_gpu(s, w_dev, mbs_dev, keep_all=True)
+    finally:
+        mlp.mlp_set_split_tail(True)
+    for j in range(s.k):
+        for k in ("U", "Y", "O", "dX"):
+            a, b = to_f64(g_outs[j][k]), to_f64(u_outs[j][k])
+            # the same fp32 sum in two orders, then one bf16 rounding: at most one bf16 step apart
+            assert np.max(np.abs(a - b)) <= 2.0 ** -7 * np.max(np.abs(b)) + 1e-30, (j, k)

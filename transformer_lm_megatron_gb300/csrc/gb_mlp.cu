@@ -37,6 +37,10 @@ namespace {
 
 // Device status word: [0] = first error code, [1] = the site that recorded it.
 __device__ int g_status_word[2];
+// Partial sums and arrival counters of the GEMMs' split tail (static, so that no
+// call allocates; the counters return to 0 after every use).
+__device__ float g_split_ws[kSplitSlots * 2 * kSplitSlotFloats];
+__device__ int g_split_flags[kSplitSlots];
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
@@ -95,6 +99,8 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;
+  float* split_ws = nullptr;   // partial sums of the GEMMs' split tail
+  int* split_flags = nullptr;
   bool gemm_attr[16] = {};  // per GEMM instantiation: dynamic smem attribute set
   int max_pairs[16] = {};   // per CTA-pair instantiation: co-resident clusters of two
 };
@@ -126,6 +132,13 @@ int device_state(DeviceState** out) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_status_word);
     if (e != cudaSuccess) return fail(MLP_ECUDA, "status word address: %s", cudaGetErrorString(e));
+    void* ws = nullptr;
+    void* flags = nullptr;
+    e = cudaGetSymbolAddress(&ws, g_split_ws);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&flags, g_split_flags);
+    if (e != cudaSuccess) return fail(MLP_ECUDA, "split-tail workspace address: %s", cudaGetErrorString(e));
+    st.split_ws = static_cast<float*>(ws);
+    st.split_flags = static_cast<int*>(flags);
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -605,6 +618,8 @@ int mlp_sync_status(void* stream) {
   if (word[0] != 0) {
     const int zero[2] = {0, 0};
     cudaMemcpy(st->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
+    // a launch that gave up may have left split-tail counters behind
+    cudaMemset(st->split_flags, 0, sizeof(int) * kSplitSlots);
     return fail(word[0], "a kernel gave up on a bounded wait (site %d)", word[1]);
   }
   return MLP_OK;
@@ -657,6 +672,12 @@ int mlp_set_cta_pair(int mode) {
 int mlp_set_dependent_launch(int enable) {
   if (enable != 0 && enable != 1) return fail(MLP_EINVAL, "mlp_set_dependent_launch: %d not in {0, 1}", enable);
   g_pdl.store(enable, std::memory_order_relaxed);
+  return MLP_OK;
+}
+
+int mlp_set_split_tail(int enable) {
+  if (enable != 0 && enable != 1) return fail(MLP_EINVAL, "mlp_set_split_tail: %d not in {0, 1}", enable);
+  g_split_tail.store(enable, std::memory_order_relaxed);
   return MLP_OK;
 }
 

@@ -18,6 +18,7 @@ std::atomic<int> g_pair_mode{-1};
 // paced epilogue stores, and late dependency waits of mlp_bwd's last GEMMs.
 std::atomic<int> g_epi_pace{1};
 std::atomic<int> g_late_wait{1};
+std::atomic<int> g_split_tail{1};
 
 // Late dependency waits pay only for short GEMMs: there the next launch's tiles
 // fill the partial last wave and the pipeline drain of the one before.  Tiles are
@@ -124,15 +125,35 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
   epx.pace = g_epi_pace.load(std::memory_order_relaxed);
   late_wait = late_wait && g_late_wait.load(std::memory_order_relaxed) &&
               2.0 * (double)M * (double)N * (double)K * (double)batch <= kLateWaitMaxFlop;
+  // Split tail: when the last wave of tiles fills at most half of the CTAs (pairs),
+  // its tiles run as two half-reductions each, so that wave takes half as long.
+  // Only for bf16 epilogues of plain GEMMs with a reduction of 16 k-blocks or more,
+  // and never in a late-waiting launch (the workspace is shared by all launches,
+  // which therefore must not overlap while they use it).
+  const int units = PAIR ? st->max_pairs[slot] : st->sms;
+  epx.split_base = (int)tiles;
+  epx.split_ws = nullptr;
+  epx.split_flags = nullptr;
+  int64_t items = tiles;
+  if (!BATCHED && causal == kCausalNone && !epi_f32_out(ep.kind) && !late_wait &&
+      g_split_tail.load(std::memory_order_relaxed) && (K + kBK - 1) / kBK >= 16) {
+    const int64_t rem = tiles % units;
+    if (rem > 0 && 2 * rem <= units && rem * (PAIR ? 2 : 1) * 4 <= kSplitSlots) {
+      epx.split_base = (int)(tiles - rem);
+      epx.split_ws = st->split_ws;
+      epx.split_flags = st->split_flags;
+      items = tiles + rem;
+    }
+  }
   const int ts = trace_pre(stream);
   cudaError_t e;
   if (PAIR) {
-    const int pairs = (int)(tiles < st->max_pairs[slot] ? tiles : st->max_pairs[slot]);
+    const int pairs = (int)(items < st->max_pairs[slot] ? items : st->max_pairs[slot]);
     e = launch_kernel(kern, dim3(2 * (unsigned)pairs), dim3(kGemmThreads), Cfg::kSmemBytes, stream, 2, 1, mA, mB, mC,
                       mO0, mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
                       st->status);
   } else {
-    const int grid = (int)(tiles < st->sms ? tiles : st->sms);
+    const int grid = (int)(items < st->sms ? items : st->sms);
     e = launch_kernel(kern, dim3((unsigned)grid), dim3(kGemmThreads), Cfg::kSmemBytes, stream, 1, 1, mA, mB, mC, mO0,
                       mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
                       st->status);

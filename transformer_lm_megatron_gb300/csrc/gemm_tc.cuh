@@ -100,7 +100,17 @@ struct EpiParams {
   float alpha;                // scale of kEpiScaleMask
   DropoutParams drop;
   int pace;                   // 1: pace the output stores against the next tile's main loop
+  // Split tail (bf16 epilogues of plain GEMMs): tiles [split_base, num_tiles) are
+  // computed as two halves of the reduction by two CTAs (pairs); each half writes
+  // its fp32 partial to split_ws and counts itself in split_flags, and the second
+  // to arrive adds the other's partial to its own and runs the epilogue.
+  int split_base;
+  float* split_ws;            // kSplitSlots x 2 halves x (32 x 256) fp32
+  int* split_flags;           // kSplitSlots counters, 0 between launches
 };
+// Slots of the split tail: (tile, CTA of the pair, epilogue warp) triples.
+constexpr int kSplitSlots = 304;
+constexpr int kSplitSlotFloats = 32 * 256;
 
 __device__ __forceinline__ void ld_bf16x8(const uint16_t* p, float (&v)[8]) {
   const uint4 q = *reinterpret_cast<const uint4*>(p);
@@ -322,7 +332,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     skip |= *reinterpret_cast<volatile int*>(peer_skip);
     cluster_sync();  // the peer has read s_skip before anything else touches it
   }
-  const int tile_end = skip ? 0 : num_tiles;
+  // Work items: tiles [0, split_base) whole, then each tile of the split tail as two
+  // items, one per half of its reduction (see EpiParams).
+  const int split_base = (!BATCHED && ep.split_ws != nullptr) ? min(ep.split_base, num_tiles) : num_tiles;
+  const int num_items = split_base + 2 * (num_tiles - split_base);
+  const int item_end = skip ? 0 : num_items;
 
   auto tile_origin = [&](int tile, int& m0, int& n0, int& hb, int& sb) {
     hb = 0;
@@ -364,6 +378,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   };
 
+  // Decodes a work item into its tile's origin, its k-block range and its half
+  // of the reduction (-1: the whole tile); false if the tile is skipped.
+  auto item_info = [&](int item, int& m0, int& n0, int& hb, int& sb, int& kb0, int& kb1, int& half) -> bool {
+    int tile = item;
+    half = -1;
+    if (item >= split_base) {
+      tile = split_base + ((item - split_base) >> 1);
+      half = (item - split_base) & 1;
+    }
+    tile_origin(tile, m0, n0, hb, sb);
+    if (skip_tile(m0, n0)) return false;
+    kb_range(m0, kb0, kb1);
+    if (half >= 0) {
+      const int mid = (kb0 + kb1) / 2;
+      if (half == 0)
+        kb1 = mid;
+      else
+        kb0 = mid;
+    }
+    return true;
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -377,12 +413,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = unit; tile < tile_end && ok; tile += num_units) {
-        int m0, n0, hb, sb;
-        tile_origin(tile, m0, n0, hb, sb);
-        if (skip_tile(m0, n0)) continue;
-        int kb0, kb1;
-        kb_range(m0, kb0, kb1);
+      for (int item = unit; item < item_end && ok; item += num_units) {
+        int m0, n0, hb, sb, kb0, kb1, half;
+        if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
         const int b_n0 = n0 + (PAIR ? (int)rank * Cfg::kBLoadN : 0);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1)) {
@@ -493,12 +526,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int tile = unit; tile < tile_end && ok; tile += num_units) {
-        int m0, n0, hb, sb;
-        tile_origin(tile, m0, n0, hb, sb);
-        if (skip_tile(m0, n0)) continue;
-        int kb0, kb1;
-        kb_range(m0, kb0, kb1);
+      for (int item = unit; item < item_end && ok; item += num_units) {
+        int m0, n0, hb, sb, kb0, kb1, half;
+        if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
         if (!(PAIR ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1) : mbar_wait(&acc_empty[acc], acc_phase ^ 1))) {
           record_status(status, kStatusTimeout, 3);
           break;
@@ -562,24 +592,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t kb_end = 0;  // the producer's k-block count once this tile's copies are all issued
-    for (int tile = unit; tile < tile_end; tile += num_units) {
-      int m0, n0, hb, sb;
-      tile_origin(tile, m0, n0, hb, sb);
-      if (skip_tile(m0, n0)) continue;
-      int kb0, kb1;
-      kb_range(m0, kb0, kb1);
+    for (int item = unit; item < item_end; item += num_units) {
+      int m0, n0, hb, sb, kb0, kb1, half;
+      if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
       kb_end += (uint32_t)max(kb1 - kb0, 0);
-      // Reduction length of this CTA's next tile, whose main loop these stores
-      // are spread over (0: no next tile, the stores go out at once).
+      // Reduction length of this CTA's next item, whose main loop these stores
+      // are spread over (0: no next item, the stores go out at once).
       uint32_t nkb_next = 0;
-      if (tile + num_units < tile_end) {
-        int m1, n1, hb1, sb1;
-        tile_origin(tile + num_units, m1, n1, hb1, sb1);
-        if (!skip_tile(m1, n1)) {
-          int a0, a1;
-          kb_range(m1, a0, a1);
-          nkb_next = (uint32_t)max(a1 - a0, 0);
-        }
+      if (item + num_units < item_end) {
+        int m1, n1, hb1, sb1, a0, a1, half1;
+        if (item_info(item + num_units, m1, n1, hb1, sb1, a0, a1, half1)) nkb_next = (uint32_t)max(a1 - a0, 0);
       }
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
@@ -588,8 +610,38 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tc_fence_after();
       const int64_t row = (int64_t)m0 + row_in_tile;
       const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+      // Split tail: publish this half's partial (this warp's 32 rows x 256 columns),
+      // count this half in; the half that arrives second adds the other's partial
+      // to its own below and writes the output, the first is done.  fp32 addition
+      // commutes, so the result does not depend on which half arrives second.
+      const float* other = nullptr;
+      bool finisher = true;
+      if (half >= 0) {
+        const int slot = (((item - split_base) >> 1) * (PAIR ? 2 : 1) + (int)rank) * 4 + quarter;
+        float* mine = ep.split_ws + (size_t)(2 * slot + half) * kSplitSlotFloats + lane * 256;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kBN; c0 += 32) {
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c0, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(mine + c0 + 4 * j) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        }
+        __threadfence();
+        __syncwarp();
+        int before = 0;
+        if (lane == 0) before = atomicAdd(&ep.split_flags[slot], 1);
+        before = __shfl_sync(0xffffffffu, before, 0);
+        finisher = before == 1;
+        if (finisher) {
+          __threadfence();
+          if (lane == 0) ep.split_flags[slot] = 0;  // ready for the next launch
+          other = ep.split_ws + (size_t)(2 * slot + (half ^ 1)) * kSplitSlotFloats + lane * 256;
+        }
+      }
+#pragma unroll 1
+      for (int c0 = 0; c0 < (finisher ? kBN : 0); c0 += 32) {
         if (ep.pace && nkb_next > 0 && c0 > 0) {
           // Pace the output: column block c0 / 32 (of 8) leaves once the producer is
           // about (3 / 32) * (c0 / 32) of the way through the next tile's copies, so
@@ -607,6 +659,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c0, r);
         tmem_ld_wait();
+        if (other != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 o = __ldcg(reinterpret_cast<const float4*>(other + c0 + 4 * j));
+            r[4 * j] = __float_as_uint(__uint_as_float(r[4 * j]) + o.x);
+            r[4 * j + 1] = __float_as_uint(__uint_as_float(r[4 * j + 1]) + o.y);
+            r[4 * j + 2] = __float_as_uint(__uint_as_float(r[4 * j + 2]) + o.z);
+            r[4 * j + 3] = __float_as_uint(__uint_as_float(r[4 * j + 3]) + o.w);
+          }
+        }
         if (tma_out) {
           // Warp-uniform: this warp's 32 rows x 32 columns go out as one TMA box;
           // rows >= M and columns >= N are clipped by the tensor map.
