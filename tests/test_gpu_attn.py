@@ -44,6 +44,8 @@ def _weights(h, gen, std=0.02):
     (256, 256, 4, 2, 128, 2),     # two sequences, d = 64, two accumulated micro-batches
     (272, 320, 4, 4, 136, 1),     # ragged: d = 80, seq_len 136 (tails in every GEMM)
     (2048, 2048, 16, 8, 1024, 1),  # two sequences of 1024, d = 128, eight slices
+    (2048, 256, 2, 2, 2048, 1),    # one sequence of 2048: the longest rows the warp-per-row softmax holds
+    (2304, 128, 2, 1, 2304, 1),    # rows past 2048 columns: the CTA-per-row softmax
 ])
 def test_attention_block_full_parity(T, h, nh, t, L, k):
     p, seed = 0.1, 1234

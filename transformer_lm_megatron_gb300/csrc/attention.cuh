@@ -4,7 +4,8 @@
 //           1/sqrt(d) scale and -inf above the causal diagonal; P is stored bf16.
 // Backward: dS[r, :] = P (dP - sum_j dP_j P_j) * alpha, with alpha = 1/sqrt(d);
 //           dS is stored bf16.
-// One CTA per row (grid-stride over rows); rows of `cols` elements, cols % 8 == 0.
+// Rows of `cols` elements, cols % 8 == 0: one warp per row for cols <= 2048 (the
+// row held in registers, read once), else one CTA per row (grid-stride over rows).
 // The rows are causal: row r is query q = r % cols of its sequence and only keys
 // c <= q carry probability.  Both kernels read the first roundup8(q + 1) entries
 // (the scores beyond q there are -inf, the gradients finite) and write exact zeros
@@ -119,6 +120,124 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
       o.y = pack_bf16x2(bf16lo(q.y) * (a.z - delta) * alpha, bf16hi(q.y) * (a.w - delta) * alpha);
       o.z = pack_bf16x2(bf16lo(q.z) * (b.x - delta) * alpha, bf16hi(q.z) * (b.y - delta) * alpha);
       o.w = pack_bf16x2(bf16lo(q.w) * (b.z - delta) * alpha, bf16hi(q.w) * (b.w - delta) * alpha);
+      *reinterpret_cast<uint4*>(dS + r * cols + c) = o;
+    }
+  }
+}
+
+// Warp-per-row variants for rows of up to 256 * CHUNKS columns: each lane keeps its
+// 8-column pieces of the row in registers, so the row is read from HBM once, and
+// the reductions are warp shuffles in a fixed butterfly order (deterministic).
+// A CTA works on kSoftmaxRowsPerCta rows at a time.
+constexpr int kSoftmaxRowsPerCta = 8;
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int CHUNKS>
+__global__ void __launch_bounds__(kSoftmaxRowsPerCta * 32)
+    k_softmax_rows_warp(const float* __restrict__ S, uint16_t* __restrict__ P, int64_t rows, int cols) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * kSoftmaxRowsPerCta;
+  for (int64_t r = (int64_t)blockIdx.x * kSoftmaxRowsPerCta + (threadIdx.x >> 5); r < rows; r += stride) {
+    const float* s = S + r * cols;
+    uint16_t* p = P + r * cols;
+    const int active = ((int)(r % cols) + 8) & ~7;  // roundup8(q + 1)
+    float v[CHUNKS][8];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < CHUNKS; ++i) {
+      const int c = (i * 32 + lane) * 8;
+      if (c < active) {
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(s + c));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(s + c) + 1);
+        v[i][0] = a.x; v[i][1] = a.y; v[i][2] = a.z; v[i][3] = a.w;
+        v[i][4] = b.x; v[i][5] = b.y; v[i][6] = b.z; v[i][7] = b.w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) mx = fmaxf(mx, v[i][j]);
+      }
+    }
+    mx = warp_max(mx);
+    float sum = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CHUNKS; ++i) {
+      if ((i * 32 + lane) * 8 < active) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          v[i][j] = __expf(v[i][j] - mx);
+          sum += v[i][j];
+        }
+      }
+    }
+    const float inv = 1.0f / warp_sum(sum);
+#pragma unroll
+    for (int i = 0; i < CHUNKS; ++i) {
+      const int c = (i * 32 + lane) * 8;
+      if (c >= cols) continue;
+      uint4 o = make_uint4(0, 0, 0, 0);
+      if (c < active) {
+        o.x = pack_bf16x2(v[i][0] * inv, v[i][1] * inv);
+        o.y = pack_bf16x2(v[i][2] * inv, v[i][3] * inv);
+        o.z = pack_bf16x2(v[i][4] * inv, v[i][5] * inv);
+        o.w = pack_bf16x2(v[i][6] * inv, v[i][7] * inv);
+      }
+      *reinterpret_cast<uint4*>(p + c) = o;
+    }
+  }
+}
+
+template <int CHUNKS>
+__global__ void __launch_bounds__(kSoftmaxRowsPerCta * 32)
+    k_softmax_bwd_rows_warp(const uint16_t* __restrict__ P, const float* __restrict__ dP, uint16_t* __restrict__ dS,
+                            int64_t rows, int cols, float alpha) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * kSoftmaxRowsPerCta;
+  for (int64_t r = (int64_t)blockIdx.x * kSoftmaxRowsPerCta + (threadIdx.x >> 5); r < rows; r += stride) {
+    const uint16_t* p = P + r * cols;
+    const float* g = dP + r * cols;
+    const int active = ((int)(r % cols) + 8) & ~7;  // roundup8(q + 1)
+    uint4 pq[CHUNKS];
+    float gv[CHUNKS][8];
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < CHUNKS; ++i) {
+      const int c = (i * 32 + lane) * 8;
+      if (c < active) {
+        pq[i] = *reinterpret_cast<const uint4*>(p + c);
+        const float4 a = __ldcs(reinterpret_cast<const float4*>(g + c));
+        const float4 b = __ldcs(reinterpret_cast<const float4*>(g + c) + 1);
+        gv[i][0] = a.x; gv[i][1] = a.y; gv[i][2] = a.z; gv[i][3] = a.w;
+        gv[i][4] = b.x; gv[i][5] = b.y; gv[i][6] = b.z; gv[i][7] = b.w;
+        dot += bf16lo(pq[i].x) * gv[i][0] + bf16hi(pq[i].x) * gv[i][1] + bf16lo(pq[i].y) * gv[i][2] +
+               bf16hi(pq[i].y) * gv[i][3] + bf16lo(pq[i].z) * gv[i][4] + bf16hi(pq[i].z) * gv[i][5] +
+               bf16lo(pq[i].w) * gv[i][6] + bf16hi(pq[i].w) * gv[i][7];
+      }
+    }
+    const float delta = warp_sum(dot);
+#pragma unroll
+    for (int i = 0; i < CHUNKS; ++i) {
+      const int c = (i * 32 + lane) * 8;
+      if (c >= cols) continue;
+      uint4 o = make_uint4(0, 0, 0, 0);
+      if (c < active) {
+        o.x = pack_bf16x2(bf16lo(pq[i].x) * (gv[i][0] - delta) * alpha, bf16hi(pq[i].x) * (gv[i][1] - delta) * alpha);
+        o.y = pack_bf16x2(bf16lo(pq[i].y) * (gv[i][2] - delta) * alpha, bf16hi(pq[i].y) * (gv[i][3] - delta) * alpha);
+        o.z = pack_bf16x2(bf16lo(pq[i].z) * (gv[i][4] - delta) * alpha, bf16hi(pq[i].z) * (gv[i][5] - delta) * alpha);
+        o.w = pack_bf16x2(bf16lo(pq[i].w) * (gv[i][6] - delta) * alpha, bf16hi(pq[i].w) * (gv[i][7] - delta) * alpha);
+      }
       *reinterpret_cast<uint4*>(dS + r * cols + c) = o;
     }
   }

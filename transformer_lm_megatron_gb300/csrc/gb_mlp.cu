@@ -231,6 +231,17 @@ int launch_check(cudaError_t e, const char* what) {
   return MLP_OK;
 }
 
+template <int CHUNKS>
+cudaError_t softmax_warp_launch(DeviceState* st, bool backward, const uint16_t* P_in, const float* F_in, uint16_t* out,
+                                int64_t rows, int cols, float alpha, cudaStream_t s) {
+  const int64_t ctas_needed = (rows + kSoftmaxRowsPerCta - 1) / kSoftmaxRowsPerCta;
+  const int64_t blocks = ctas_needed < (int64_t)st->sms * 8 ? ctas_needed : (int64_t)st->sms * 8;
+  const dim3 grid((unsigned)blocks), block(kSoftmaxRowsPerCta * 32);
+  return backward ? launch_kernel(k_softmax_bwd_rows_warp<CHUNKS>, grid, block, 0, s, 1, 1, P_in, F_in, out, rows,
+                                  cols, alpha)
+                  : launch_kernel(k_softmax_rows_warp<CHUNKS>, grid, block, 0, s, 1, 1, F_in, out, rows, cols);
+}
+
 }  // namespace
 
 namespace gbmlp {
@@ -426,11 +437,16 @@ int softmax_launch(DeviceState* st, bool backward, const uint16_t* P_in, const f
                    int cols, float alpha, cudaStream_t s) {
   int64_t blocks = rows < (int64_t)st->sms * 16 ? rows : (int64_t)st->sms * 16;
   const int ts = trace_pre(s);
+  const int chunks = (cols + 255) / 256;
   const cudaError_t e =
-      backward ? launch_kernel(k_softmax_bwd_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, P_in,
-                               F_in, out, rows, cols, alpha)
-               : launch_kernel(k_softmax_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, F_in, out,
-                               rows, cols);
+      chunks <= 1   ? softmax_warp_launch<1>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
+      : chunks <= 2 ? softmax_warp_launch<2>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
+      : chunks <= 4 ? softmax_warp_launch<4>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
+      : chunks <= 8 ? softmax_warp_launch<8>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
+      : backward    ? launch_kernel(k_softmax_bwd_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1,
+                                    P_in, F_in, out, rows, cols, alpha)
+                    : launch_kernel(k_softmax_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, F_in,
+                                    out, rows, cols);
   trace_post(ts, s, kTraceSoftmax, rows, cols, 0);
   return launch_check(e, backward ? "softmax backward" : "softmax");
 }
