@@ -4,10 +4,11 @@
 //   (+)= adds to the accumulator, or overwrites it for the first micro-batch of a step
 //   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
 //
-// Column sums are deterministic: a cluster of 8 CTAs owns 64 columns, each CTA
-// a fixed eighth of the rows; each of a CTA's 64 row-lanes sums a fixed row
-// subset, the lanes' sums are added in a fixed order, and CTA 0 adds the 8 CTAs'
-// sums in rank order through distributed shared memory.  Loads and stores are
+// Column sums are deterministic: a cluster of 1 to 8 CTAs (enough for the grid to
+// fill the GPU) owns 64 columns, each CTA a fixed share of the rows; each of a
+// CTA's 64 row-lanes sums a fixed row subset, the lanes' sums are added in a fixed
+// order, and CTA 0 adds the CTAs' sums in rank order through distributed shared
+// memory.  Loads and stores are
 // 16-byte vectors; a warp covers four 128-byte row segments per instruction.
 #pragma once
 #include <cstdint>
@@ -20,11 +21,11 @@ namespace gbmlp {
 constexpr int kColRowLanes = 64;                 // threads along the rows of a column strip
 constexpr int kColThreads = 8 * kColRowLanes;    // 8 column groups (8 bf16 = 16 B each) x row lanes
 constexpr int kColsPerCta = 64;
-constexpr int kColRowSplit = 8;                  // CTAs of a cluster, each summing 1/8 of the rows
+constexpr int kColRowSplitMax = 8;               // most CTAs of a cluster splitting the rows
 
-// Deterministic column sums over a cluster of kColRowSplit CTAs (grid y = rank):
+// Deterministic column sums over a cluster of gridDim.y CTAs (grid y = rank):
 // every CTA reduces its row range to 64 partial sums in a fixed order, then CTA 0
-// adds the 8 partial vectors, in rank order, through distributed shared memory.
+// adds the partial vectors, in rank order, through distributed shared memory.
 // part is [kColRowLanes][kColsPerCta + 1]; returns the total for thread
 // threadIdx.x < kColsPerCta of CTA rank 0 (0 elsewhere).
 __device__ __forceinline__ float cluster_colsum(float (*part)[kColsPerCta + 1], float* psum) {
@@ -36,7 +37,7 @@ __device__ __forceinline__ float cluster_colsum(float (*part)[kColsPerCta + 1], 
   cluster_sync();  // every CTA's partial vector is complete
   float tot = 0.0f;
   if (cluster_ctarank() == 0 && threadIdx.x < kColsPerCta) {
-    for (unsigned r = 0; r < kColRowSplit; ++r) {
+    for (unsigned r = 0; r < gridDim.y; ++r) {
       const float* peer = static_cast<const float*>(__cluster_map_shared_rank(static_cast<void*>(psum), r));
       tot += peer[threadIdx.x];
     }
@@ -46,7 +47,7 @@ __device__ __forceinline__ float cluster_colsum(float (*part)[kColsPerCta + 1], 
 }
 
 // dZ = dO * keep * scale (rounded to bf16); db[c] (+)= sum over rows of the rounded dZ.
-// Grid (ceil(cols / 64), kColRowSplit), clusters of (1, kColRowSplit, 1).
+// Grid (ceil(cols / 64), split), clusters of (1, split, 1), split <= kColRowSplitMax.
 __global__ void __launch_bounds__(kColThreads)
     k_dropout_bwd_colsum(const uint16_t* __restrict__ dO, uint16_t* __restrict__ dZ, float* __restrict__ db,
                          int64_t rows, int cols, DropoutParams drop, int accumulate) {
@@ -57,8 +58,8 @@ __global__ void __launch_bounds__(kColThreads)
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
   const int col = blockIdx.x * kColsPerCta + cg * 8;
-  const int64_t r_begin = rows * (int64_t)blockIdx.y / kColRowSplit;
-  const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / kColRowSplit;
+  const int64_t r_begin = rows * (int64_t)blockIdx.y / gridDim.y;
+  const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / gridDim.y;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (col < cols) {
     for (int64_t r = r_begin + rl; r < r_end; r += kColRowLanes) {
@@ -101,8 +102,8 @@ __global__ void __launch_bounds__(kColThreads)
   const int cg = threadIdx.x & 7;
   const int rl = threadIdx.x >> 3;
   const int col = blockIdx.x * kColsPerCta + cg * 8;
-  const int64_t r_begin = rows * (int64_t)blockIdx.y / kColRowSplit;
-  const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / kColRowSplit;
+  const int64_t r_begin = rows * (int64_t)blockIdx.y / gridDim.y;
+  const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / gridDim.y;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
   if (col < cols) {
     for (int64_t r = r_begin + rl; r < r_end; r += kColRowLanes) {

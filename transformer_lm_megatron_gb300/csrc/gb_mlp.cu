@@ -224,6 +224,16 @@ int check_ptrs(const char* what, std::initializer_list<const void*> ptrs) {
   return MLP_OK;
 }
 
+// CTAs per column block of a column sum: the fewest (1, 2, 4 or 8) that give the
+// grid about four CTAs per SM; the choice depends on the shape only, so the
+// summation order, and the result, is fixed for a shape.
+unsigned colsum_split(const DeviceState* st, int64_t cols) {
+  const int64_t blocks = (cols + kColsPerCta - 1) / kColsPerCta;
+  unsigned split = 1;
+  while (split < (unsigned)kColRowSplitMax && blocks * split < 4 * (int64_t)st->sms) split *= 2;
+  return split;
+}
+
 int launch_check(cudaError_t e, const char* what) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -334,8 +344,9 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   if (first_call) {
     // B1: dZ = dO * m / (1 - p), db += sum_tok dZ
     const int ts = trace_pre(s);
-    const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, kColRowSplit),
-                                        dim3(kColThreads), 0, s, 1, kColRowSplit, dO, dZ, db, tokens, h, drop,
+    const unsigned split = colsum_split(st, h);
+    const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, split),
+                                        dim3(kColThreads), 0, s, 1, split, dO, dZ, db, tokens, h, drop,
                                         accumulate ? 1 : 0);
     trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
     rc = launch_check(e, "dropout backward");
@@ -355,8 +366,9 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     if (rc) return rc;
     // da_i += sum_tok dU_i
     const int ts = trace_pre(s);
-    const cudaError_t e = launch_kernel(k_colsum_bf16, dim3((f + kColsPerCta - 1) / kColsPerCta, kColRowSplit),
-                                        dim3(kColThreads), 0, s, 1, kColRowSplit, (const uint16_t*)(dU + c),
+    const unsigned split = colsum_split(st, f);
+    const cudaError_t e = launch_kernel(k_colsum_bf16, dim3((f + kColsPerCta - 1) / kColsPerCta, split),
+                                        dim3(kColThreads), 0, s, 1, split, (const uint16_t*)(dU + c),
                                         (int64_t)ffn, da + c, tokens, f, accumulate ? 1 : 0);
     trace_post(ts, s, kTraceColsum, tokens, f, 0);
     rc = launch_check(e, "bias-gradient column sum");
@@ -558,8 +570,9 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   {
     const DropoutParams drop = make_dropout(p, seed, token_offset, h);
     const int ts = trace_pre(s);
-    const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, kColRowSplit),
-                                        dim3(kColThreads), 0, s, 1, kColRowSplit, dOut, dZ, dbo, tokens, h, drop, acc);
+    const unsigned split = colsum_split(st, h);
+    const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, split),
+                                        dim3(kColThreads), 0, s, 1, split, dOut, dZ, dbo, tokens, h, drop, acc);
     trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
     rc = launch_check(e, "dropout backward");
     if (rc) return rc;
@@ -601,8 +614,9 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   {
     const int ts = trace_pre(s);
     const cudaError_t e =
-        launch_kernel(k_colsum_bf16, dim3((unsigned)((h3 + kColsPerCta - 1) / kColsPerCta), kColRowSplit),
-                      dim3(kColThreads), 0, s, 1, kColRowSplit, (const uint16_t*)dQKV, (int64_t)h3, dbqkv, tokens,
+        launch_kernel(k_colsum_bf16, dim3((unsigned)((h3 + kColsPerCta - 1) / kColsPerCta), colsum_split(st, h3)),
+                      dim3(kColThreads), 0, s, 1, colsum_split(st, h3), (const uint16_t*)dQKV, (int64_t)h3, dbqkv,
+                      tokens,
                       (int)h3, acc);
     trace_post(ts, s, kTraceColsum, tokens, h3, 0);
     rc = launch_check(e, "bias-gradient column sum");
