@@ -184,6 +184,34 @@ def oracle_sample(wl, sample_inputs):
     return dt, 12 * X64.shape[0] * wl.h * A_i.shape[1]
 
 
+def sampled_parity(wl, weights, X, dO, buf, stream, n_rows=4):
+    """Max |gpu - oracle| / max |oracle| per output over ``n_rows`` token rows of one
+    micro-batch at the benchmarked size (the float64 oracle in its bf16-mirroring
+    mode, full rows over all slices; the fp32 weight gradients need every token and
+    are left to the test suite)."""
+    import numpy as np
+    import torch
+    from oracle import mlp_oracle as orc
+    from transformer_lm_megatron_gb300 import mlp
+    rows = np.unique(np.linspace(0, wl.tokens - 1, n_rows).astype(np.int64))
+    mlp.block_step(wl, weights, X, dO, buf, token_offset=0, slice_mode="all", stream=stream, accumulate=False)
+    torch.cuda.synchronize()
+    bits = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)  # noqa: E731
+    ridx = torch.as_tensor(rows, device=X.device)
+    A, a, B, b = weights
+    ref = orc.rows_fwd_bwd(rows, orc.Bf16Matrix(bits(X)), orc.Bf16Matrix(bits(dO)), orc.Bf16Matrix(bits(A)),
+                           orc.bf16_to_f64(bits(a)), orc.Bf16Matrix(bits(B)), orc.bf16_to_f64(bits(b)), wl.t, wl.p,
+                           wl.seed, 0, mirror=True)
+    out = {"rows": [int(r) for r in rows], "oracle_mode": "bf16-mirroring, float64"}
+    for name in ("U", "Y", "O", "dZ", "dU", "dX"):
+        g = orc.bf16_to_f64(bits(getattr(buf, name).index_select(0, ridx)))
+        r = ref[name]
+        den = float(np.max(np.abs(r)))
+        out[f"{name}_max_rel_err"] = float(np.max(np.abs(g - r)) / den) if den > 0 else float(np.max(np.abs(g)))
+    out["tolerance"] = 1e-2
+    return out
+
+
 def workload_config(wl, slice_mode, world):
     """The `config` object of the JSON line (the same for both arms)."""
     return {"workload": wl.name, "tokens": wl.tokens, "h": wl.h, "ffn": wl.ffn, "t": wl.t,
@@ -575,6 +603,7 @@ def run_ours(args, wl, rank, world, dist):
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
                "sample": f"{args.cpu_tokens} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, "
                          f"float64 numpy, {dt:.1f} s"}
+        cpu["parity"] = sampled_parity(wl, weights, mbs[0][0], mbs[0][1], buf, stream)
     if adam is not None:
         adam["peak_GBps"] = peaks["hbm_gbs"]
         adam["frac"] = adam["achieved_GBps"] / peaks["hbm_gbs"]
