@@ -262,6 +262,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* in_full = mma_done + 2;  // per epilogue warp, 2: prefetched input boxes (GeLU' epilogue)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -291,6 +292,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(mma_done, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(&in_full[i], 1);
     fence_mbar_init();
   }
   const bool tma_out = epi_f32_out(ep.kind);
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tma_prefetch_desc(&tmC);
     } else {
       tma_prefetch_desc(&tmO0);
-      if (ep.kind == kEpiGelu) tma_prefetch_desc(&tmO1);
+      if (ep.kind == kEpiGelu || ep.kind == kEpiDGelu) tma_prefetch_desc(&tmO1);
     }
   }
   if (warp == 1) {
@@ -592,6 +594,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t kb_end = 0;  // the producer's k-block count once this tile's copies are all issued
+    // GeLU' epilogue: the warp's 32 x 32 box of the stored U is fetched by TMA (map
+    // tmO1) one column block ahead, into the second half of an output buffer, so
+    // the epilogue never waits on scattered global loads.
+    const bool prefetch_in = !BATCHED && ep.kind == kEpiDGelu;
+    uint64_t* my_in_full = in_full + 2 * (warp - 2);
+    uint32_t n_in = 0;  // input boxes this warp has requested
+    auto in_box = [&](uint32_t i) { return my_out + (i & 1) * kOutBoxBytes + kOutBoxBf16Bytes; };
+    auto request_in = [&](int x, int y) {
+      if (lane == 0) {
+        uint64_t* bar = &my_in_full[n_in & 1];
+        mbar_arrive_expect_tx(bar, kOutBoxBf16Bytes);
+        tma_load_2d(in_box(n_in), &tmO1, bar, x, y, 0, false);
+      }
+      ++n_in;
+    };
     for (int item = unit; item < item_end; item += num_units) {
       int m0, n0, hb, sb, kb0, kb1, half;
       if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
@@ -603,6 +620,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int m1, n1, hb1, sb1, a0, a1, half1;
         if (item_info(item + num_units, m1, n1, hb1, sb1, a0, a1, half1)) nkb_next = (uint32_t)max(a1 - a0, 0);
       }
+      // column blocks of this warp that produce output (the rest are clipped)
+      const bool rows_in = m0 + quarter * 32 < M;
+      uint32_t n_in_used = n_in;  // index of the next input box to consume
+      const bool in_first = prefetch_in && rows_in && n0 < N;
+      if (in_first) request_in(n0, m0 + quarter * 32);
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
@@ -638,6 +660,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __threadfence();
           if (lane == 0) ep.split_flags[slot] = 0;  // ready for the next launch
           other = ep.split_ws + (size_t)(2 * slot + (half ^ 1)) * kSplitSlotFloats + lane * 256;
+        } else if (in_first) {
+          // no output from this half: retire the input box requested for it
+          const uint32_t i = n_in_used++;
+          if (!mbar_wait(&my_in_full[i & 1], (i >> 1) & 1)) record_status(status, kStatusTimeout, 7);
         }
       }
 #pragma unroll 1
@@ -711,6 +737,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j)  // kEpiStore: the only bf16 epilogue of batched GEMMs
               o0[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          } else if (prefetch_in) {
+            // next column block's U box first, then this one's (already requested)
+            if (c0 + 32 < kBN && n0 + c0 + 32 < N) request_in(n0 + c0 + 32, m0 + quarter * 32);
+            const uint32_t i = n_in_used++;
+            if (!mbar_wait(&my_in_full[i & 1], (i >> 1) & 1)) record_status(status, kStatusTimeout, 7);
+            const uint8_t* ub = in_box(i);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint4 q = *reinterpret_cast<const uint4*>(ub + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
+              const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float a0 = __uint_as_float(r[8 * j + 2 * k]) * gelu_prime_f(bf16lo(w4[k]));
+                const float a1 = __uint_as_float(r[8 * j + 2 * k + 1]) * gelu_prime_f(bf16hi(w4[k]));
+                o0[4 * j + k] = pack_bf16x2(a0, a1);
+              }
+            }
           } else {
             epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1);
           }
