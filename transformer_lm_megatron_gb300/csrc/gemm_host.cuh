@@ -187,7 +187,8 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
   } else {
     rc = make_out_map_bf16(&mO0, ep.out0, N, M, ep.ld);
     if (rc) return rc;
-    if (ep.kind == kEpiDGelu) {  // the stored U, read by the epilogue through TMA
+    if (ep.in0 != nullptr && (ep.kind == kEpiDGelu || ep.kind == kEpiDropRes || ep.kind == kEpiResAdd)) {
+      // the bf16 input (U, R or dO), read by the epilogue through TMA
       rc = make_out_map_bf16(&mO1, ep.in0, N, M, ep.ld);
       if (rc) return rc;
     }

@@ -127,14 +127,28 @@ __device__ __forceinline__ void ld_f32x8(const float* p, float (&v)[8]) {
   v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 
+// The bf16 input in0 of lane `lane`'s row, columns [8 g, 8 g + 8) of a 32 x 32
+// box staged by TMA with the 64-byte swizzle.
+__device__ __forceinline__ void ld_staged_bf16x8(const uint8_t* box, int lane, int g, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(box + lane * 64 + ((g ^ ((lane >> 1) & 3)) << 4));
+  v[0] = bf16lo(q.x); v[1] = bf16hi(q.x);
+  v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+  v[4] = bf16lo(q.z); v[5] = bf16hi(q.z);
+  v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+}
+
 // One thread, one row, 32 accumulator columns [col0, col0 + 32); N % 8 == 0.
 // Computes the bf16 output(s) of the fused epilogue, packed two per word:
 // o0 = U / O / dU / dX, o1 = Y (GeLU only).  Inputs are read only inside the
 // tensor (row < M, col < N); out-of-range lanes produce values the TMA store clips.
+// in_box: in0's 32 x 32 box for this warp and column block, staged in shared
+// memory by TMA (zero outside the tensor), or null to read in0 from global memory.
 template <int KIND>
 __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
-                                                int M, int N, uint32_t (&o0)[16], uint32_t (&o1)[16]) {
+                                                int M, int N, uint32_t (&o0)[16], uint32_t (&o1)[16],
+                                                const uint8_t* in_box) {
   const bool row_ok = row < M;
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
     const int col = col0 + 8 * g;
@@ -166,7 +180,10 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row
         for (int j = 0; j < 8; ++j) v[j] = z[j] + v[j];
       }
       if (col_ok) ld_bf16x8(ep.bias + col, bb);
-      if (ok) ld_bf16x8(ep.in0 + off, res);
+      if (in_box != nullptr)
+        ld_staged_bf16x8(in_box, lane, g, res);
+      else if (ok)
+        ld_bf16x8(ep.in0 + off, res);
       const uint32_t keep = dropout_keep8(ep.drop, row, col);
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] = res[j] + (((keep >> j) & 1u) ? (v[j] + bb[j]) * ep.drop.scale : 0.0f);
@@ -174,7 +191,10 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row
       for (int j = 0; j < 4; ++j) o0[4 * g + j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
     } else if constexpr (KIND == kEpiDGelu) {
       float u[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-      if (ok) ld_bf16x8(ep.in0 + off, u);
+      if (in_box != nullptr)
+        ld_staged_bf16x8(in_box, lane, g, u);
+      else if (ok)
+        ld_bf16x8(ep.in0 + off, u);
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[j] *= gelu_prime_f(u[j]);
 #pragma unroll
@@ -194,9 +214,12 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] = z[j] + v[j];
       }
-      if (ok && ep.in0 != nullptr) {
+      if (ep.in0 != nullptr && (ok || in_box != nullptr)) {
         float res[8];
-        ld_bf16x8(ep.in0 + off, res);
+        if (in_box != nullptr)
+          ld_staged_bf16x8(in_box, lane, g, res);
+        else
+          ld_bf16x8(ep.in0 + off, res);
 #pragma unroll
         for (int j = 0; j < 8; ++j) v[j] += res[j];
       }
@@ -207,14 +230,15 @@ __device__ __forceinline__ void epilogue_values(const EpiParams& ep, int64_t row
 }
 
 __device__ __forceinline__ void epilogue_dispatch(const EpiParams& ep, int64_t row, int col0, const uint32_t (&r)[32],
-                                                  int M, int N, uint32_t (&o0)[16], uint32_t (&o1)[16]) {
+                                                  int M, int N, uint32_t (&o0)[16], uint32_t (&o1)[16],
+                                                  const uint8_t* in_box) {
   switch (ep.kind) {
-    case kEpiGelu: epilogue_values<kEpiGelu>(ep, row, col0, r, M, N, o0, o1); break;
-    case kEpiDropRes: epilogue_values<kEpiDropRes>(ep, row, col0, r, M, N, o0, o1); break;
-    case kEpiDGelu: epilogue_values<kEpiDGelu>(ep, row, col0, r, M, N, o0, o1); break;
-    case kEpiBias: epilogue_values<kEpiBias>(ep, row, col0, r, M, N, o0, o1); break;
-    case kEpiStore: epilogue_values<kEpiStore>(ep, row, col0, r, M, N, o0, o1); break;
-    default: epilogue_values<kEpiResAdd>(ep, row, col0, r, M, N, o0, o1); break;
+    case kEpiGelu: epilogue_values<kEpiGelu>(ep, row, col0, r, M, N, o0, o1, in_box); break;
+    case kEpiDropRes: epilogue_values<kEpiDropRes>(ep, row, col0, r, M, N, o0, o1, in_box); break;
+    case kEpiDGelu: epilogue_values<kEpiDGelu>(ep, row, col0, r, M, N, o0, o1, in_box); break;
+    case kEpiBias: epilogue_values<kEpiBias>(ep, row, col0, r, M, N, o0, o1, in_box); break;
+    case kEpiStore: epilogue_values<kEpiStore>(ep, row, col0, r, M, N, o0, o1, in_box); break;
+    default: epilogue_values<kEpiResAdd>(ep, row, col0, r, M, N, o0, o1, in_box); break;
   }
 }
 
@@ -303,7 +327,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tma_prefetch_desc(&tmC);
     } else {
       tma_prefetch_desc(&tmO0);
-      if (ep.kind == kEpiGelu || ep.kind == kEpiDGelu) tma_prefetch_desc(&tmO1);
+      if (ep.kind == kEpiGelu || (ep.in0 != nullptr && (ep.kind == kEpiDGelu || ep.kind == kEpiDropRes ||
+                                                          ep.kind == kEpiResAdd)))
+        tma_prefetch_desc(&tmO1);
     }
   }
   if (warp == 1) {
@@ -594,10 +620,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t kb_end = 0;  // the producer's k-block count once this tile's copies are all issued
-    // GeLU' epilogue: the warp's 32 x 32 box of the stored U is fetched by TMA (map
+    // Epilogues with a bf16 input in0 (U for GeLU', R for dropout + residual, dO
+    // for the input gradient): the warp's 32 x 32 box of it is fetched by TMA (map
     // tmO1) one column block ahead, into the second half of an output buffer, so
     // the epilogue never waits on scattered global loads.
-    const bool prefetch_in = !BATCHED && ep.kind == kEpiDGelu;
+    const bool prefetch_in = !BATCHED && ep.in0 != nullptr &&
+                             (ep.kind == kEpiDGelu || ep.kind == kEpiDropRes || ep.kind == kEpiResAdd);
     uint64_t* my_in_full = in_full + 2 * (warp - 2);
     uint32_t n_in = 0;  // input boxes this warp has requested
     auto in_box = [&](uint32_t i) { return my_out + (i & 1) * kOutBoxBytes + kOutBoxBf16Bytes; };
@@ -737,25 +765,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int j = 0; j < 16; ++j)  // kEpiStore: the only bf16 epilogue of batched GEMMs
               o0[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-          } else if (prefetch_in) {
-            // next column block's U box first, then this one's (already requested)
-            if (c0 + 32 < kBN && n0 + c0 + 32 < N) request_in(n0 + c0 + 32, m0 + quarter * 32);
-            const uint32_t i = n_in_used++;
-            if (!mbar_wait(&my_in_full[i & 1], (i >> 1) & 1)) record_status(status, kStatusTimeout, 7);
-            const uint8_t* ub = in_box(i);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint4 q = *reinterpret_cast<const uint4*>(ub + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
-              const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const float a0 = __uint_as_float(r[8 * j + 2 * k]) * gelu_prime_f(bf16lo(w4[k]));
-                const float a1 = __uint_as_float(r[8 * j + 2 * k + 1]) * gelu_prime_f(bf16hi(w4[k]));
-                o0[4 * j + k] = pack_bf16x2(a0, a1);
-              }
-            }
           } else {
-            epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1);
+            const uint8_t* ib = nullptr;
+            if (prefetch_in) {
+              // next column block's input box first, then this one's (already requested)
+              if (c0 + 32 < kBN && n0 + c0 + 32 < N) request_in(n0 + c0 + 32, m0 + quarter * 32);
+              const uint32_t i = n_in_used++;
+              if (!mbar_wait(&my_in_full[i & 1], (i >> 1) & 1)) record_status(status, kStatusTimeout, 7);
+              ib = in_box(i);
+            }
+            epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1, ib);
           }
           uint8_t* box0 = my_out + (n_out & 1) * (2 * kOutBoxBf16Bytes);
           uint8_t* box1 = box0 + kOutBoxBf16Bytes;
