@@ -245,8 +245,9 @@ int mlp_set_dependent_launch(int enable);
  * those tiles is computed as two halves of its reduction by two pairs, whose fp32
  * partial sums are added (in either order: the sum is the same) before the
  * epilogue.  Results stay deterministic; they differ from the unsplit ones only by
- * fp32 summation order.  The partial sums use 20 MB of statically allocated device
- * memory.  Returns MLP_OK or MLP_EINVAL.
+ * fp32 summation order.  The partial sums use statically allocated device memory,
+ * one 20 MB region per stream for the first 4 streams that launch such a GEMM;
+ * GEMMs on further streams run unsplit.  Returns MLP_OK or MLP_EINVAL.
  */
 int mlp_set_split_tail(int enable);
 

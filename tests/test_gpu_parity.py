@@ -278,3 +278,33 @@ def test_split_tail_full_parity(tokens, h, ffn, t, cta_pair_mode):
             a, b = to_f64(g_outs[j][k]), to_f64(u_outs[j][k])
             # the same fp32 sum in two orders, then one bf16 rounding: at most one bf16 step apart
             assert np.max(np.abs(a - b)) <= 2.0 ** -7 * np.max(np.abs(b)) + 1e-30, (j, k)
+
+
+def test_split_tail_on_concurrent_streams():
+    """Two blocks whose GEMMs split their tail run at the same time on two streams:
+    each stream has its own workspace region, so both match their one-stream runs
+    bit for bit."""
+    shapes = [Shape(tokens=512, h=1280, ffn=2048, t=1, k=2, p=0.1),
+              Shape(tokens=512, h=1280, ffn=2048, t=1, k=2, p=0.1, seed=99)]  # another dropout mask
+    s = shapes[0]
+    cases = [make_case(sh) for sh in shapes]
+    ref = []
+    for sh, (w_dev, mbs_dev, _, _) in zip(shapes, cases):
+        outs, grads = run_gpu(sh, w_dev, mbs_dev, keep_all=True)
+        ref.append((outs, grads))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    bufs = [mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t) for _ in cases]
+    torch.cuda.synchronize()
+    for rep in range(3):
+        for j in range(s.k):
+            for c, (w_dev, mbs_dev, _, _) in enumerate(cases):
+                X, dO = mbs_dev[j]
+                mlp.block_step(shapes[c], w_dev, X, dO, bufs[c], token_offset=j * s.tokens, stream=streams[c],
+                               accumulate=j > 0)
+        torch.cuda.synchronize()
+        assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+        for c in range(2):
+            for k in ("U", "Y", "O", "dZ", "dU", "dX"):
+                assert torch.equal(getattr(bufs[c], k).cpu(), ref[c][0][-1][k]), (rep, c, k)
+            for k in ("dA", "da", "dB", "db"):
+                assert torch.equal(getattr(bufs[c], k).cpu(), ref[c][1][k]), (rep, c, k)

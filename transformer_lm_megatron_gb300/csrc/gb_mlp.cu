@@ -38,9 +38,12 @@ namespace {
 // Device status word: [0] = first error code, [1] = the site that recorded it.
 __device__ int g_status_word[2];
 // Partial sums and arrival counters of the GEMMs' split tail (static, so that no
-// call allocates; the counters return to 0 after every use).
-__device__ float g_split_ws[kSplitSlots * 2 * kSplitSlotFloats];
-__device__ int g_split_flags[kSplitSlots];
+// call allocates; the counters return to 0 after every use), one region per
+// stream for up to kSplitRegions streams: launches on one stream never use the
+// region at the same time (see gemm), launches on different streams may.
+constexpr int kSplitRegions = 4;
+__device__ float g_split_ws[kSplitRegions][kSplitSlots * 2 * kSplitSlotFloats];
+__device__ int g_split_flags[kSplitRegions][kSplitSlots];
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
@@ -99,8 +102,10 @@ struct DeviceState {
   bool ready = false;
   int sms = 0;
   int* status = nullptr;
-  float* split_ws = nullptr;   // partial sums of the GEMMs' split tail
+  float* split_ws = nullptr;   // partial sums of the GEMMs' split tail, kSplitRegions regions
   int* split_flags = nullptr;
+  cudaStream_t split_owner[kSplitRegions] = {};  // the stream each region belongs to
+  int split_regions_used = 0;
   bool gemm_attr[16] = {};  // per GEMM instantiation: dynamic smem attribute set
   int max_pairs[16] = {};   // per CTA-pair instantiation: co-resident clusters of two
 };
@@ -156,6 +161,18 @@ int device_state(DeviceState** out) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The split-tail region of `stream` (assigned on first use), or -1 once all
+// regions belong to other streams; GEMMs on such a stream run without the split.
+std::mutex g_split_mu;
+int split_region(DeviceState* st, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_split_mu);
+  for (int r = 0; r < st->split_regions_used; ++r)
+    if (st->split_owner[r] == stream) return r;
+  if (st->split_regions_used == kSplitRegions) return -1;
+  st->split_owner[st->split_regions_used] = stream;
+  return st->split_regions_used++;
+}
 
 // Programmatic dependent launch: a kernel may be scheduled while the previous
 // kernel on its stream drains, running its prologue (barriers, TMEM, descriptor
@@ -649,7 +666,7 @@ int mlp_sync_status(void* stream) {
     const int zero[2] = {0, 0};
     cudaMemcpy(st->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
     // a launch that gave up may have left split-tail counters behind
-    cudaMemset(st->split_flags, 0, sizeof(int) * kSplitSlots);
+    cudaMemset(st->split_flags, 0, sizeof(int) * kSplitSlots * kSplitRegions);
     return fail(word[0], "a kernel gave up on a bounded wait (site %d)", word[1]);
   }
   return MLP_OK;

@@ -128,8 +128,8 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
   // Split tail: when the last wave of tiles fills at most half of the CTAs (pairs),
   // its tiles run as two half-reductions each, so that wave takes half as long.
   // Only for bf16 epilogues of plain GEMMs with a reduction of 16 k-blocks or more,
-  // and never in a late-waiting launch (the workspace is shared by all launches,
-  // which therefore must not overlap while they use it).
+  // and never in a late-waiting launch: the workspace region is shared by all
+  // launches on the stream, which therefore must not overlap while they use it.
   const int units = PAIR ? st->max_pairs[slot] : st->sms;
   epx.split_base = (int)tiles;
   epx.split_ws = nullptr;
@@ -138,10 +138,12 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
   if (!BATCHED && causal == kCausalNone && !epi_f32_out(ep.kind) && !late_wait &&
       g_split_tail.load(std::memory_order_relaxed) && (K + kBK - 1) / kBK >= 16) {
     const int64_t rem = tiles % units;
-    if (rem > 0 && 2 * rem <= units && rem * (PAIR ? 2 : 1) * 4 <= kSplitSlots) {
+    const int region = (rem > 0 && 2 * rem <= units && rem * (PAIR ? 2 : 1) * 4 <= kSplitSlots)
+                           ? split_region(st, stream) : -1;
+    if (region >= 0) {
       epx.split_base = (int)(tiles - rem);
-      epx.split_ws = st->split_ws;
-      epx.split_flags = st->split_flags;
+      epx.split_ws = st->split_ws + (size_t)region * kSplitSlots * 2 * kSplitSlotFloats;
+      epx.split_flags = st->split_flags + (size_t)region * kSplitSlots;
       items = tiles + rem;
     }
   }
