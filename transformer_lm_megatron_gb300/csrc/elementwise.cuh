@@ -4,8 +4,8 @@
 //   (+)= adds to the accumulator, or overwrites it for the first micro-batch of a step
 //   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
 //
-// Column sums are deterministic: a cluster of 1 to 8 CTAs (enough for the grid to
-// fill the GPU) owns 64 columns, each CTA a fixed share of the rows; each of a
+// Column sums are deterministic: a cluster of 1 to 8 CTAs (as many as keep the
+// grid resident in one wave) owns 64 columns, each CTA a fixed share of the rows; each of a
 // CTA's 64 row-lanes sums a fixed row subset, the lanes' sums are added in a fixed
 // order, and CTA 0 adds the CTAs' sums in rank order through distributed shared
 // memory.  Loads and stores are
@@ -61,25 +61,34 @@ __global__ void __launch_bounds__(kColThreads)
   const int64_t r_begin = rows * (int64_t)blockIdx.y / gridDim.y;
   const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / gridDim.y;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (col < cols) {
-    for (int64_t r = r_begin + rl; r < r_end; r += kColRowLanes) {
-      const int64_t off = r * cols + col;
-      const uint4 q = *reinterpret_cast<const uint4*>(dO + off);
-      float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
-                    bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
-      const uint32_t keep = dropout_keep8(drop, r, col);
+  // One row's 8 columns: dZ out, the rounded values into the running sums.
+  auto row_step = [&](int64_t r, const uint4& q) {
+    float v[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
+                  bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
+    const uint32_t keep = dropout_keep8(drop, r, col);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        v[j] = round_bf16_f(((keep >> j) & 1u) ? v[j] * drop.scale : 0.0f);
-        s[j] += v[j];
-      }
-      uint4 o;
-      o.x = pack_bf16x2(v[0], v[1]);
-      o.y = pack_bf16x2(v[2], v[3]);
-      o.z = pack_bf16x2(v[4], v[5]);
-      o.w = pack_bf16x2(v[6], v[7]);
-      *reinterpret_cast<uint4*>(dZ + off) = o;
+    for (int j = 0; j < 8; ++j) {
+      v[j] = round_bf16_f(((keep >> j) & 1u) ? v[j] * drop.scale : 0.0f);
+      s[j] += v[j];
     }
+    uint4 o;
+    o.x = pack_bf16x2(v[0], v[1]);
+    o.y = pack_bf16x2(v[2], v[3]);
+    o.z = pack_bf16x2(v[4], v[5]);
+    o.w = pack_bf16x2(v[6], v[7]);
+    *reinterpret_cast<uint4*>(dZ + r * cols + col) = o;
+  };
+  if (col < cols) {
+    // rows in increasing order, the loads of four rows issued together
+    int64_t r = r_begin + rl;
+    for (; r + 3 * kColRowLanes < r_end; r += 4 * kColRowLanes) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const uint4*>(dO + (r + u * kColRowLanes) * cols + col);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) row_step(r + u * kColRowLanes, q[u]);
+    }
+    for (; r < r_end; r += kColRowLanes) row_step(r, *reinterpret_cast<const uint4*>(dO + r * cols + col));
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[rl][cg * 8 + j] = s[j];
@@ -105,14 +114,23 @@ __global__ void __launch_bounds__(kColThreads)
   const int64_t r_begin = rows * (int64_t)blockIdx.y / gridDim.y;
   const int64_t r_end = rows * (int64_t)(blockIdx.y + 1) / gridDim.y;
   float s[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  auto add_row = [&](const uint4& q) {
+    s[0] += bf16lo(q.x); s[1] += bf16hi(q.x);
+    s[2] += bf16lo(q.y); s[3] += bf16hi(q.y);
+    s[4] += bf16lo(q.z); s[5] += bf16hi(q.z);
+    s[6] += bf16lo(q.w); s[7] += bf16hi(q.w);
+  };
   if (col < cols) {
-    for (int64_t r = r_begin + rl; r < r_end; r += kColRowLanes) {
-      const uint4 q = *reinterpret_cast<const uint4*>(x + r * ld + col);
-      s[0] += bf16lo(q.x); s[1] += bf16hi(q.x);
-      s[2] += bf16lo(q.y); s[3] += bf16hi(q.y);
-      s[4] += bf16lo(q.z); s[5] += bf16hi(q.z);
-      s[6] += bf16lo(q.w); s[7] += bf16hi(q.w);
+    // rows in increasing order, the loads of four rows issued together
+    int64_t r = r_begin + rl;
+    for (; r + 3 * kColRowLanes < r_end; r += 4 * kColRowLanes) {
+      uint4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const uint4*>(x + (r + u * kColRowLanes) * ld + col);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) add_row(q[u]);
     }
+    for (; r < r_end; r += kColRowLanes) add_row(*reinterpret_cast<const uint4*>(x + r * ld + col));
   }
 #pragma unroll
   for (int j = 0; j < 8; ++j) part[rl][cg * 8 + j] = s[j];

@@ -241,10 +241,32 @@ int check_ptrs(const char* what, std::initializer_list<const void*> ptrs) {
   return MLP_OK;
 }
 
-// CTAs per column block of a column sum: the fewest (1, 2, 4 or 8) that give the
-// grid about four CTAs per SM; the choice depends on the shape only, so the
-// summation order, and the result, is fixed for a shape.
-unsigned colsum_split(const DeviceState* st, int64_t cols) {
+// CTAs per column block of the (memory-bound) column sum: the most (1, 2, 4 or 8)
+// for which the whole grid is resident at once (a second, partial wave would take
+// as long as the first); the choice depends on the shape and the device only, so
+// the summation order, and the result, is fixed for a shape.
+template <typename Kernel>
+unsigned colsum_split(const DeviceState* st, int64_t cols, Kernel kernel) {
+  static int per_sm = 0;  // per kernel (each kernel has its own signature, hence instantiation)
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kColThreads, 0) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    per_sm = n;
+  }
+  const int64_t blocks = (cols + kColsPerCta - 1) / kColsPerCta;
+  const int64_t resident = (int64_t)per_sm * st->sms;
+  unsigned split = 1;
+  while (split < (unsigned)kColRowSplitMax && blocks * split * 2 <= resident) split *= 2;
+  return split;
+}
+
+// CTAs per column block of the dropout backward, whose mask hashing makes it
+// arithmetic-bound: the fewest (1, 2, 4 or 8) that give at least four CTAs per SM
+// (measured on the MT-NLG layer: 114 us with one wave of 320 CTAs, 99 us with 640).
+unsigned dropout_bwd_split(const DeviceState* st, int64_t cols) {
   const int64_t blocks = (cols + kColsPerCta - 1) / kColsPerCta;
   unsigned split = 1;
   while (split < (unsigned)kColRowSplitMax && blocks * split < 4 * (int64_t)st->sms) split *= 2;
@@ -361,7 +383,7 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   if (first_call) {
     // B1: dZ = dO * m / (1 - p), db += sum_tok dZ
     const int ts = trace_pre(s);
-    const unsigned split = colsum_split(st, h);
+    const unsigned split = dropout_bwd_split(st, h);
     const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, split),
                                         dim3(kColThreads), 0, s, 1, split, dO, dZ, db, tokens, h, drop,
                                         accumulate ? 1 : 0);
@@ -383,7 +405,7 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     if (rc) return rc;
     // da_i += sum_tok dU_i
     const int ts = trace_pre(s);
-    const unsigned split = colsum_split(st, f);
+    const unsigned split = colsum_split(st, f, k_colsum_bf16);
     const cudaError_t e = launch_kernel(k_colsum_bf16, dim3((f + kColsPerCta - 1) / kColsPerCta, split),
                                         dim3(kColThreads), 0, s, 1, split, (const uint16_t*)(dU + c),
                                         (int64_t)ffn, da + c, tokens, f, accumulate ? 1 : 0);
@@ -587,7 +609,7 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   {
     const DropoutParams drop = make_dropout(p, seed, token_offset, h);
     const int ts = trace_pre(s);
-    const unsigned split = colsum_split(st, h);
+    const unsigned split = dropout_bwd_split(st, h);
     const cudaError_t e = launch_kernel(k_dropout_bwd_colsum, dim3((h + kColsPerCta - 1) / kColsPerCta, split),
                                         dim3(kColThreads), 0, s, 1, split, dOut, dZ, dbo, tokens, h, drop, acc);
     trace_post(ts, s, kTraceDropBwd, tokens, h, 0);
@@ -631,8 +653,8 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   {
     const int ts = trace_pre(s);
     const cudaError_t e =
-        launch_kernel(k_colsum_bf16, dim3((unsigned)((h3 + kColsPerCta - 1) / kColsPerCta), colsum_split(st, h3)),
-                      dim3(kColThreads), 0, s, 1, colsum_split(st, h3), (const uint16_t*)dQKV, (int64_t)h3, dbqkv,
+        launch_kernel(k_colsum_bf16, dim3((unsigned)((h3 + kColsPerCta - 1) / kColsPerCta), colsum_split(st, h3, k_colsum_bf16)),
+                      dim3(kColThreads), 0, s, 1, colsum_split(st, h3, k_colsum_bf16), (const uint16_t*)dQKV, (int64_t)h3, dbqkv,
                       tokens,
                       (int)h3, acc);
     trace_post(ts, s, kTraceColsum, tokens, h3, 0);
