@@ -178,8 +178,12 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
  *   per sequence and head: dV = P^T dO; dP = dO V^T; dS = P (dP - rowsum(dP P)) / sqrt(d);
  *   dQ = dS K; dK = dS^T Q;  dWqkv = X^T dQKV; dbqkv = sum dQKV;
  *   dX = [dOut +] dQKV Wqkv^T   (operator f; residual_grad selects the dOut term)
- * dZ, dO [tokens, h] and dS (P's shape) are bf16 workspaces, dP an fp32 workspace of
- * P's shape, dQKV [tokens, 3h] bf16, dX [tokens, h] bf16.  Returns MLP_OK or an error.
+ * rowsum(dP P) is taken as rowsum(dO * O), the same quantity (P V = O), and dP is
+ * never stored: the product dO V^T goes straight into dS in the GEMM's epilogue.
+ * dZ, dO [tokens, h] and dS (P's shape) are bf16 workspaces (dS is written only in
+ * the 256 x 256 tiles on or below the causal diagonal, the only ones read back),
+ * dP an fp32 workspace of at least n_seq * nh * seq_len floats (the row sums),
+ * dQKV [tokens, 3h] bf16, dX [tokens, h] bf16.  Returns MLP_OK or an error.
  */
 int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
              int residual_grad, int accumulate, const mlp_bf16* dOut, const mlp_bf16* X, const mlp_bf16* Wqkv,

@@ -1,15 +1,15 @@
-// Row-wise softmax kernels of the attention core (HBM-bound).
+// Row-wise kernels of the attention core (HBM-bound).
 //
-// Forward:  P[r, :] = softmax(S[r, :]) for scores S (fp32) that already carry the
+// Softmax:  P[r, :] = softmax(S[r, :]) for scores S (fp32) that already carry the
 //           1/sqrt(d) scale and -inf above the causal diagonal; P is stored bf16.
-// Backward: dS[r, :] = P (dP - sum_j dP_j P_j) * alpha, with alpha = 1/sqrt(d);
-//           dS is stored bf16.
 // Rows of `cols` elements, cols % 8 == 0: one warp per row for cols <= 2048 (the
 // row held in registers, read once), else one CTA per row (grid-stride over rows).
 // The rows are causal: row r is query q = r % cols of its sequence and only keys
-// c <= q carry probability.  Both kernels read the first roundup8(q + 1) entries
-// (the scores beyond q there are -inf, the gradients finite) and write exact zeros
-// for the rest of the row, so the masked half of S and dP is never read.
+// c <= q carry probability.  The kernels read the first roundup8(q + 1) entries
+// (the scores beyond q there are -inf) and write exact zeros for the rest of the
+// row, so the masked half of S is never read.
+// Softmax gradient: the row sums delta = sum_k P dP = dO . O (k_attn_delta); the
+// rest, dS = P (dO V^T - delta) / sqrt(d), is the epilogue of the dO V^T GEMM.
 #pragma once
 #include <cstdint>
 
@@ -88,43 +88,6 @@ __global__ void __launch_bounds__(kSoftmaxThreads)
   }
 }
 
-__global__ void __launch_bounds__(kSoftmaxThreads)
-    k_softmax_bwd_rows(const uint16_t* __restrict__ P, const float* __restrict__ dP, uint16_t* __restrict__ dS,
-                       int64_t rows, int cols, float alpha) {
-  __shared__ float red[kSoftmaxThreads / 32];
-  grid_dependency_wait();
-  grid_launch_dependents();
-  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
-    const uint16_t* p = P + r * cols;
-    const float* g = dP + r * cols;
-    const int active = ((int)(r % cols) + 8) & ~7;  // roundup8(q + 1)
-    float dot = 0.0f;
-    for (int c = threadIdx.x * 8; c < active; c += kSoftmaxThreads * 8) {
-      const uint4 q = *reinterpret_cast<const uint4*>(p + c);
-      const float4 a = reinterpret_cast<const float4*>(g + c)[0];
-      const float4 b = reinterpret_cast<const float4*>(g + c)[1];
-      dot += bf16lo(q.x) * a.x + bf16hi(q.x) * a.y + bf16lo(q.y) * a.z + bf16hi(q.y) * a.w + bf16lo(q.z) * b.x +
-             bf16hi(q.z) * b.y + bf16lo(q.w) * b.z + bf16hi(q.w) * b.w;
-    }
-    const float delta = block_reduce_sum(dot, red);
-    for (int c = threadIdx.x * 8; c < cols; c += kSoftmaxThreads * 8) {
-      if (c >= active) {
-        *reinterpret_cast<uint4*>(dS + r * cols + c) = make_uint4(0, 0, 0, 0);
-        continue;
-      }
-      const uint4 q = *reinterpret_cast<const uint4*>(p + c);
-      const float4 a = reinterpret_cast<const float4*>(g + c)[0];
-      const float4 b = reinterpret_cast<const float4*>(g + c)[1];
-      uint4 o;
-      o.x = pack_bf16x2(bf16lo(q.x) * (a.x - delta) * alpha, bf16hi(q.x) * (a.y - delta) * alpha);
-      o.y = pack_bf16x2(bf16lo(q.y) * (a.z - delta) * alpha, bf16hi(q.y) * (a.w - delta) * alpha);
-      o.z = pack_bf16x2(bf16lo(q.z) * (b.x - delta) * alpha, bf16hi(q.z) * (b.y - delta) * alpha);
-      o.w = pack_bf16x2(bf16lo(q.w) * (b.z - delta) * alpha, bf16hi(q.w) * (b.w - delta) * alpha);
-      *reinterpret_cast<uint4*>(dS + r * cols + c) = o;
-    }
-  }
-}
-
 // Warp-per-row variants for rows of up to 256 * CHUNKS columns: each lane keeps its
 // 8-column pieces of the row in registers, so the row is read from HBM once, and
 // the reductions are warp shuffles in a fixed butterfly order (deterministic).
@@ -197,48 +160,38 @@ __global__ void __launch_bounds__(kSoftmaxRowsPerCta * 32)
   }
 }
 
-template <int CHUNKS>
-__global__ void __launch_bounds__(kSoftmaxRowsPerCta * 32)
-    k_softmax_bwd_rows_warp(const uint16_t* __restrict__ P, const float* __restrict__ dP, uint16_t* __restrict__ dS,
-                            int64_t rows, int cols, float alpha) {
+// delta[s, j, q] = sum_c dO[s L + q, j d + c] * O[s L + q, j d + c], the row sums
+// sum_k P dP of the softmax gradient (sum_k P_qk (dO_q . V_k) = dO_q . O_q), in fp32.
+// One warp per (token, head): lanes take 8-column pieces, then a fixed-order
+// butterfly sum.  d % 8 == 0.
+constexpr int kDeltaWarps = 8;
+
+__global__ void __launch_bounds__(kDeltaWarps * 32)
+    k_attn_delta(const uint16_t* __restrict__ dO, const uint16_t* __restrict__ O, float* __restrict__ delta,
+                 int64_t tokens, int h, int nh, int L) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int lane = threadIdx.x & 31;
-  const int64_t stride = (int64_t)gridDim.x * kSoftmaxRowsPerCta;
-  for (int64_t r = (int64_t)blockIdx.x * kSoftmaxRowsPerCta + (threadIdx.x >> 5); r < rows; r += stride) {
-    const uint16_t* p = P + r * cols;
-    const float* g = dP + r * cols;
-    const int active = ((int)(r % cols) + 8) & ~7;  // roundup8(q + 1)
-    uint4 pq[CHUNKS];
-    float gv[CHUNKS][8];
-    float dot = 0.0f;
-#pragma unroll
-    for (int i = 0; i < CHUNKS; ++i) {
-      const int c = (i * 32 + lane) * 8;
-      if (c < active) {
-        pq[i] = *reinterpret_cast<const uint4*>(p + c);
-        const float4 a = __ldcs(reinterpret_cast<const float4*>(g + c));
-        const float4 b = __ldcs(reinterpret_cast<const float4*>(g + c) + 1);
-        gv[i][0] = a.x; gv[i][1] = a.y; gv[i][2] = a.z; gv[i][3] = a.w;
-        gv[i][4] = b.x; gv[i][5] = b.y; gv[i][6] = b.z; gv[i][7] = b.w;
-        dot += bf16lo(pq[i].x) * gv[i][0] + bf16hi(pq[i].x) * gv[i][1] + bf16lo(pq[i].y) * gv[i][2] +
-               bf16hi(pq[i].y) * gv[i][3] + bf16lo(pq[i].z) * gv[i][4] + bf16hi(pq[i].z) * gv[i][5] +
-               bf16lo(pq[i].w) * gv[i][6] + bf16hi(pq[i].w) * gv[i][7];
-      }
+  const int d = h / nh;
+  const int64_t n = tokens * nh;
+  const int64_t stride = (int64_t)gridDim.x * kDeltaWarps;
+  for (int64_t w = (int64_t)blockIdx.x * kDeltaWarps + (threadIdx.x >> 5); w < n; w += stride) {
+    const int64_t tok = w / nh;
+    const int j = (int)(w - tok * nh);
+    const uint16_t* a = dO + tok * h + (int64_t)j * d;
+    const uint16_t* b = O + tok * h + (int64_t)j * d;
+    float acc = 0.0f;
+    for (int c = lane * 8; c < d; c += 256) {
+      const uint4 qa = *reinterpret_cast<const uint4*>(a + c);
+      const uint4 qb = *reinterpret_cast<const uint4*>(b + c);
+      acc += bf16lo(qa.x) * bf16lo(qb.x) + bf16hi(qa.x) * bf16hi(qb.x) + bf16lo(qa.y) * bf16lo(qb.y) +
+             bf16hi(qa.y) * bf16hi(qb.y) + bf16lo(qa.z) * bf16lo(qb.z) + bf16hi(qa.z) * bf16hi(qb.z) +
+             bf16lo(qa.w) * bf16lo(qb.w) + bf16hi(qa.w) * bf16hi(qb.w);
     }
-    const float delta = warp_sum(dot);
-#pragma unroll
-    for (int i = 0; i < CHUNKS; ++i) {
-      const int c = (i * 32 + lane) * 8;
-      if (c >= cols) continue;
-      uint4 o = make_uint4(0, 0, 0, 0);
-      if (c < active) {
-        o.x = pack_bf16x2(bf16lo(pq[i].x) * (gv[i][0] - delta) * alpha, bf16hi(pq[i].x) * (gv[i][1] - delta) * alpha);
-        o.y = pack_bf16x2(bf16lo(pq[i].y) * (gv[i][2] - delta) * alpha, bf16hi(pq[i].y) * (gv[i][3] - delta) * alpha);
-        o.z = pack_bf16x2(bf16lo(pq[i].z) * (gv[i][4] - delta) * alpha, bf16hi(pq[i].z) * (gv[i][5] - delta) * alpha);
-        o.w = pack_bf16x2(bf16lo(pq[i].w) * (gv[i][6] - delta) * alpha, bf16hi(pq[i].w) * (gv[i][7] - delta) * alpha);
-      }
-      *reinterpret_cast<uint4*>(dS + r * cols + c) = o;
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      const int64_t sq = tok / L, q = tok - sq * L;
+      delta[(sq * nh + j) * L + q] = acc;
     }
   }
 }

@@ -281,14 +281,11 @@ int launch_check(cudaError_t e, const char* what) {
 }
 
 template <int CHUNKS>
-cudaError_t softmax_warp_launch(DeviceState* st, bool backward, const uint16_t* P_in, const float* F_in, uint16_t* out,
-                                int64_t rows, int cols, float alpha, cudaStream_t s) {
+cudaError_t softmax_warp_launch(DeviceState* st, const float* S, uint16_t* P, int64_t rows, int cols, cudaStream_t s) {
   const int64_t ctas_needed = (rows + kSoftmaxRowsPerCta - 1) / kSoftmaxRowsPerCta;
   const int64_t blocks = ctas_needed < (int64_t)st->sms * 8 ? ctas_needed : (int64_t)st->sms * 8;
-  const dim3 grid((unsigned)blocks), block(kSoftmaxRowsPerCta * 32);
-  return backward ? launch_kernel(k_softmax_bwd_rows_warp<CHUNKS>, grid, block, 0, s, 1, 1, P_in, F_in, out, rows,
-                                  cols, alpha)
-                  : launch_kernel(k_softmax_rows_warp<CHUNKS>, grid, block, 0, s, 1, 1, F_in, out, rows, cols);
+  return launch_kernel(k_softmax_rows_warp<CHUNKS>, dim3((unsigned)blocks), dim3(kSoftmaxRowsPerCta * 32), 0, s, 1, 1,
+                       S, P, rows, cols);
 }
 
 }  // namespace
@@ -484,22 +481,19 @@ int check_attn_shape(int h, int nh, int t, int64_t tokens, int seq_len, float p)
   return MLP_OK;
 }
 
-int softmax_launch(DeviceState* st, bool backward, const uint16_t* P_in, const float* F_in, uint16_t* out, int64_t rows,
-                   int cols, float alpha, cudaStream_t s) {
+int softmax_launch(DeviceState* st, const float* S, uint16_t* P, int64_t rows, int cols, cudaStream_t s) {
   int64_t blocks = rows < (int64_t)st->sms * 16 ? rows : (int64_t)st->sms * 16;
   const int ts = trace_pre(s);
   const int chunks = (cols + 255) / 256;
   const cudaError_t e =
-      chunks <= 1   ? softmax_warp_launch<1>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
-      : chunks <= 2 ? softmax_warp_launch<2>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
-      : chunks <= 4 ? softmax_warp_launch<4>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
-      : chunks <= 8 ? softmax_warp_launch<8>(st, backward, P_in, F_in, out, rows, cols, alpha, s)
-      : backward    ? launch_kernel(k_softmax_bwd_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1,
-                                    P_in, F_in, out, rows, cols, alpha)
-                    : launch_kernel(k_softmax_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, F_in,
-                                    out, rows, cols);
+      chunks <= 1   ? softmax_warp_launch<1>(st, S, P, rows, cols, s)
+      : chunks <= 2 ? softmax_warp_launch<2>(st, S, P, rows, cols, s)
+      : chunks <= 4 ? softmax_warp_launch<4>(st, S, P, rows, cols, s)
+      : chunks <= 8 ? softmax_warp_launch<8>(st, S, P, rows, cols, s)
+                    : launch_kernel(k_softmax_rows, dim3((unsigned)blocks), dim3(kSoftmaxThreads), 0, s, 1, 1, S, P,
+                                    rows, cols);
   trace_post(ts, s, kTraceSoftmax, rows, cols, 0);
-  return launch_check(e, backward ? "softmax backward" : "softmax");
+  return launch_check(e, "softmax");
 }
 
 int adam_step(int64_t n, const float* grad, float grad_scale, float* master, float* m, float* v, mlp_bf16* weight,
@@ -570,7 +564,7 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   rc = gemm_batched(st, {QKV, false, L, d, h3, d, L * h3}, {QKV + h, false, L, d, h3, d, L * h3},
                     {S, L, L, L, LL, nh * LL}, L, L, d, nh, ns, es, s, kTraceAttnGemm, kCausalSkipUpper);
   if (rc) return rc;
-  rc = softmax_launch(st, false, nullptr, S, P, (int64_t)ns * nh * L, L, 0.0f, s);
+  rc = softmax_launch(st, S, P, (int64_t)ns * nh * L, L, s);
   if (rc) return rc;
   // O = P V per head, written into head j's columns of O
   EpiParams eo{};
@@ -630,18 +624,33 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   ed.out0 = dO;
   rc = gemm(st, dZ, false, h, Wo, false, h, T, h, h, ed, s, kTraceAttnGemm);
   if (rc) return rc;
-  // per (sequence, head): dV = P^T dO, dP = dO V^T, dS = softmax'(P, dP) / sqrt(d), dQ = dS K, dK = dS^T Q
+  // per (sequence, head): dV = P^T dO, dS = P (dO V^T - delta) / sqrt(d) with delta = rowsum(dO * O)
+  // (fused: the product dO V^T never leaves the GEMM), dQ = dS K, dK = dS^T Q
   EpiParams est{};
   est.kind = kEpiStore;
   rc = gemm_batched(st, {P, true, L, L, L, LL, nh * LL}, {dO, true, d, L, h, d, (int64_t)L * h},
                     {dQKV + 2 * h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKFrom);
   if (rc) return rc;
-  EpiParams ef{};
-  ef.kind = kEpiF32Store;
+  float* delta = dP;  // ns * nh * L floats of the fp32 workspace
+  {
+    const int64_t warps = tokens * nh;
+    int64_t blocks = (warps + kDeltaWarps - 1) / kDeltaWarps;
+    if (blocks > (int64_t)st->sms * 16) blocks = (int64_t)st->sms * 16;
+    const int ts = trace_pre(s);
+    const cudaError_t e = launch_kernel(k_attn_delta, dim3((unsigned)blocks), dim3(kDeltaWarps * 32), 0, s, 1, 1,
+                                        (const uint16_t*)dO, (const uint16_t*)O, delta, tokens, h, nh, L);
+    trace_post(ts, s, kTraceSoftmax, tokens, h, 0);
+    rc = launch_check(e, "softmax-gradient row sums");
+    if (rc) return rc;
+  }
+  EpiParams eg{};
+  eg.kind = kEpiSoftmaxGrad;
+  eg.in0 = P;
+  eg.g_in = delta;
+  eg.ld = L;
+  eg.alpha = 1.0f / std::sqrt((float)d);
   rc = gemm_batched(st, {dO, false, L, d, h, d, (int64_t)L * h}, {QKV + 2 * h, false, L, d, h3, d, L * h3},
-                    {dP, L, L, L, LL, nh * LL}, L, L, d, nh, ns, ef, s, kTraceAttnGemm, kCausalSkipUpper);
-  if (rc) return rc;
-  rc = softmax_launch(st, true, P, dP, dS, (int64_t)ns * nh * L, L, 1.0f / std::sqrt((float)d), s);
+                    {dS, L, L, L, LL, nh * LL}, L, L, d, nh, ns, eg, s, kTraceAttnGemm, kCausalSkipUpper);
   if (rc) return rc;
   rc = gemm_batched(st, {dS, false, L, L, L, LL, nh * LL}, {QKV + h, true, d, L, h3, d, L * h3},
                     {dQKV, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKUpTo);

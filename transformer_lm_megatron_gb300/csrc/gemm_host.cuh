@@ -272,7 +272,7 @@ int make_map4(CUtensorMap* m, CUtensorMapDataType dt, int esz, const void* base,
 int gemm_batched(DeviceState* st, const BatchOperand& a, const BatchOperand& b, const BatchOutput& out, int M, int N,
                  int K, int nb_h, int nb_s, const EpiParams& ep, cudaStream_t stream, int trace_kind,
                  int causal = kCausalNone) {
-  if (!epi_tma_only(ep.kind) || ep.kind == kEpiF32Add)
+  if ((!epi_tma_only(ep.kind) && ep.kind != kEpiSoftmaxGrad) || ep.kind == kEpiF32Add)
     return fail(MLP_EUNSUPPORTED, "batched GEMM: epilogue kind %d not supported", ep.kind);
   const int mode = g_pair_mode.load(std::memory_order_relaxed);
   const bool pair = mode == 1 || (mode < 0 && M > kBM);
@@ -297,6 +297,10 @@ int gemm_batched(DeviceState* st, const BatchOperand& a, const BatchOperand& b, 
                    nb_s, out.s_stride, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
   else
     rc = make_map4(&mO0, bf, 2, out.base, out.cols, out.rows, out.ld, nb_h, out.h_stride, nb_s, out.s_stride, 32, 32,
+                   CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (rc) return rc;
+  if (ep.kind == kEpiSoftmaxGrad)  // P, laid out like the output, read by the epilogue through TMA
+    rc = make_map4(&mO1, bf, 2, ep.in0, out.cols, out.rows, out.ld, nb_h, out.h_stride, nb_s, out.s_stride, 32, 32,
                    CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
   if (rc) return rc;
   const int raster_n_fast = M > N ? 1 : 0;

@@ -54,6 +54,8 @@ constexpr uint32_t kOutStageBytes = 4 * 2 * kOutBoxBytes;  // 4 warps x 2 buffer
 // Longest an epilogue warp waits for the main loop before it stores anyway.
 constexpr uint64_t kPaceLimitNs = 200000;
 
+// Staged epilogue inputs (see the epilogue) live in the free halves of the two
+// output buffers of each epilogue warp: a ring of kInDepth = 2 boxes.
 template <bool PAIR>
 struct GemmCfg {
   static constexpr int kStages = PAIR ? 6 : 4;
@@ -61,6 +63,7 @@ struct GemmCfg {
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;       // rows of D per tile
   static constexpr uint32_t kBBytes = kBLoadN * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
+  static constexpr int kInDepth = 2;
   static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kOutStageBytes + 1024 /*align*/ + 256;
 };
 static_assert(GemmCfg<true>::kSmemBytes <= 232448 && GemmCfg<false>::kSmemBytes <= 232448, "smem budget");
@@ -76,7 +79,8 @@ enum EpiKind : int {
   kEpiResAdd = 5,    // dX = (G ? G : 0) + acc + (R ? R : 0) (bf16)
   kEpiBias = 6,      // out = acc + bias (bf16)
   kEpiStore = 7,     // out = acc (bf16)
-  kEpiScaleMask = 8  // G = (column > row ? -inf : alpha * acc) (fp32; causal attention scores)
+  kEpiScaleMask = 8,    // G = (column > row ? -inf : alpha * acc) (fp32; causal attention scores)
+  kEpiSoftmaxGrad = 9   // dS = P * (acc - delta[batch][row]) * alpha (bf16; batched; P staged by TMA)
 };
 
 // Epilogues whose output is fp32 (written through the fp32 TMA map tmC).
@@ -87,17 +91,22 @@ __host__ __device__ constexpr bool epi_f32_out(int kind) {
 __host__ __device__ constexpr bool epi_tma_only(int kind) {
   return epi_f32_out(kind) || kind == kEpiStore;
 }
+// Epilogues that read a bf16 input (in0) through a TMA-staged box (map tmO1).
+__host__ __device__ constexpr bool epi_staged_input(int kind) {
+  return kind == kEpiDGelu || kind == kEpiDropRes || kind == kEpiResAdd || kind == kEpiSoftmaxGrad;
+}
 
 struct EpiParams {
   int kind;
   int64_t ld;                 // leading dimension (elements) shared by every tensor the epilogue touches
   float* g_out;               // fp32 output (F32Store / F32Add)
-  const float* g_in;          // fp32 partial sum read by DropRes / ResAdd (may be null)
+  const float* g_in;          // fp32 partial sum read by DropRes / ResAdd (may be null); SoftmaxGrad: delta,
+                              // ld floats per batch matrix
   uint16_t* out0;             // bf16 output: U / O / dU / dX
   uint16_t* out1;             // bf16 output: Y
   const uint16_t* in0;        // bf16 input: R (DropRes, ResAdd) or U (DGelu); may be null for ResAdd
   const uint16_t* bias;       // bias vector indexed by output column
-  float alpha;                // scale of kEpiScaleMask
+  float alpha;                // scale of kEpiScaleMask and kEpiSoftmaxGrad
   DropoutParams drop;
   int pace;                   // 1: pace the output stores against the next tile's main loop
   // Split tail (bf16 epilogues of plain GEMMs): tiles [split_base, num_tiles) are
@@ -261,7 +270,7 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // l2_hints: L2 policy of the A loads (bits 0-1), the B loads (bits 2-3) and the
 // output stores (bits 4-5), an L2Hint each (kL2None: no hint).
 // BATCHED: `batch` independent GEMMs of the same M, N, K; every tensor map is 4-D
-// (x, y, hb, sb) with batch b = sb * nb_h + hb; only TMA-only epilogues.
+// (x, y, hb, sb) with batch b = sb * nb_h + hb; only TMA-only epilogues and the softmax gradient.
 // causal (batched attention products, M and N or K indexing positions in one
 // sequence): kCausalNone; kCausalSkipUpper skips tiles whose columns all lie
 // after the tile's last row (the result there is never read); kCausalKUpTo stops
@@ -275,6 +284,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                    int group, int l2_hints, int batch, int nb_h, int causal, int late_wait, int* status) {
   using Cfg = GemmCfg<PAIR>;
   constexpr int kStages = Cfg::kStages;
+  constexpr int kInDepth = Cfg::kInDepth;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -286,7 +296,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
-  uint64_t* in_full = mma_done + 2;  // per epilogue warp, 2: prefetched input boxes (GeLU' epilogue)
+  uint64_t* in_full = mma_done + 2;  // per epilogue warp, kInDepth: staged input boxes
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 8; ++i) mbar_init(&in_full[i], 1);
+    for (int i = 0; i < 4 * kInDepth; ++i) mbar_init(&in_full[i], 1);
     fence_mbar_init();
   }
   const bool tma_out = epi_f32_out(ep.kind);
@@ -327,9 +337,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tma_prefetch_desc(&tmC);
     } else {
       tma_prefetch_desc(&tmO0);
-      if (ep.kind == kEpiGelu || (ep.in0 != nullptr && (ep.kind == kEpiDGelu || ep.kind == kEpiDropRes ||
-                                                          ep.kind == kEpiResAdd)))
-        tma_prefetch_desc(&tmO1);
+      if (ep.kind == kEpiGelu || (ep.in0 != nullptr && epi_staged_input(ep.kind))) tma_prefetch_desc(&tmO1);
     }
   }
   if (warp == 1) {
@@ -621,21 +629,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint32_t acc_phase = 0;
     uint32_t kb_end = 0;  // the producer's k-block count once this tile's copies are all issued
     // Epilogues with a bf16 input in0 (U for GeLU', R for dropout + residual, dO
-    // for the input gradient): the warp's 32 x 32 box of it is fetched by TMA (map
-    // tmO1) one column block ahead, into the second half of an output buffer, so
-    // the epilogue never waits on scattered global loads.
-    const bool prefetch_in = !BATCHED && ep.in0 != nullptr &&
-                             (ep.kind == kEpiDGelu || ep.kind == kEpiDropRes || ep.kind == kEpiResAdd);
-    uint64_t* my_in_full = in_full + 2 * (warp - 2);
+    // for the input gradient, P for the softmax gradient of the attention
+    // products): the warp's 32 x 32 boxes of it are fetched by TMA (map tmO1)
+    // through a ring of kInDepth buffers (the free halves of its output buffers),
+    // kInDepth column blocks ahead, so the epilogue never waits on scattered global
+    // loads.  A buffer is refilled only after the warp has read it and written its
+    // output box.
+    const bool prefetch_in = ep.in0 != nullptr && epi_staged_input(ep.kind) && (!BATCHED || ep.kind == kEpiSoftmaxGrad);
+    uint64_t* my_in_full = in_full + kInDepth * (warp - 2);
     uint32_t n_in = 0;  // input boxes this warp has requested
-    auto in_box = [&](uint32_t i) { return my_out + (i & 1) * kOutBoxBytes + kOutBoxBf16Bytes; };
-    auto request_in = [&](int x, int y) {
+    auto in_box = [&](uint32_t i) { return my_out + (i % kInDepth) * kOutBoxBytes + kOutBoxBf16Bytes; };
+    auto request_in = [&](int x, int y, int hb, int sb) {
       if (lane == 0) {
-        uint64_t* bar = &my_in_full[n_in & 1];
+        uint64_t* bar = &my_in_full[n_in % kInDepth];
         mbar_arrive_expect_tx(bar, kOutBoxBf16Bytes);
-        tma_load_2d(in_box(n_in), &tmO1, bar, x, y, 0, false);
+        if constexpr (BATCHED)
+          tma_load_4d(in_box(n_in), &tmO1, bar, x, y, hb, sb);
+        else
+          tma_load_2d(in_box(n_in), &tmO1, bar, x, y, 0, false);
       }
       ++n_in;
+    };
+    auto wait_in = [&](uint32_t i) {
+      if (!mbar_wait(&my_in_full[i % kInDepth], (i / kInDepth) & 1)) record_status(status, kStatusTimeout, 7);
     };
     for (int item = unit; item < item_end; item += num_units) {
       int m0, n0, hb, sb, kb0, kb1, half;
@@ -650,9 +666,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // column blocks of this warp that produce output (the rest are clipped)
       const bool rows_in = m0 + quarter * 32 < M;
+      const int n_blocks = (prefetch_in && rows_in && n0 < N) ? min(kBN / 32, (N - n0 + 31) / 32) : 0;
       uint32_t n_in_used = n_in;  // index of the next input box to consume
-      const bool in_first = prefetch_in && rows_in && n0 < N;
-      if (in_first) request_in(n0, m0 + quarter * 32);
+      const int n_first = min(n_blocks, kInDepth);
+      for (int q = 0; q < n_first; ++q) request_in(n0 + 32 * q, m0 + quarter * 32, hb, sb);
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
@@ -688,10 +705,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           __threadfence();
           if (lane == 0) ep.split_flags[slot] = 0;  // ready for the next launch
           other = ep.split_ws + (size_t)(2 * slot + (half ^ 1)) * kSplitSlotFloats + lane * 256;
-        } else if (in_first) {
-          // no output from this half: retire the input box requested for it
-          const uint32_t i = n_in_used++;
-          if (!mbar_wait(&my_in_full[i & 1], (i >> 1) & 1)) record_status(status, kStatusTimeout, 7);
+        } else {
+          // no output from this half: retire the input boxes requested for it
+          for (int q = 0; q < n_first; ++q) wait_in(n_in_used++);
         }
       }
 #pragma unroll 1
@@ -761,19 +777,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         } else if (n0 + c0 < N && m0 + quarter * 32 < M) {
           // Warp-uniform, as above: bf16 output box(es) of 32 rows x 32 columns.
           uint32_t o0[16], o1[16];
+          const uint8_t* ib = nullptr;
+          if (prefetch_in) {
+            wait_in(n_in_used);
+            ib = in_box(n_in_used++);
+          }
           if constexpr (BATCHED) {
+            if (ep.kind == kEpiSoftmaxGrad) {
+              // dS = P (dP - delta) alpha, delta = sum_k P dP of this row (given)
+              const float dl = row < M ? ep.g_in[(int64_t)(sb * nb_h + hb) * ep.ld + row] : 0.0f;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)  // kEpiStore: the only bf16 epilogue of batched GEMMs
-              o0[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-          } else {
-            const uint8_t* ib = nullptr;
-            if (prefetch_in) {
-              // next column block's input box first, then this one's (already requested)
-              if (c0 + 32 < kBN && n0 + c0 + 32 < N) request_in(n0 + c0 + 32, m0 + quarter * 32);
-              const uint32_t i = n_in_used++;
-              if (!mbar_wait(&my_in_full[i & 1], (i >> 1) & 1)) record_status(status, kStatusTimeout, 7);
-              ib = in_box(i);
+              for (int g = 0; g < 4; ++g) {
+                float pv[8];
+                ld_staged_bf16x8(ib, lane, g, pv);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  o0[4 * g + j] = pack_bf16x2(pv[2 * j] * (__uint_as_float(r[8 * g + 2 * j]) - dl) * ep.alpha,
+                                              pv[2 * j + 1] * (__uint_as_float(r[8 * g + 2 * j + 1]) - dl) * ep.alpha);
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)  // kEpiStore
+                o0[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
             }
+          } else {
             epilogue_dispatch(ep, row, n0 + c0, r, M, N, o0, o1, ib);
           }
           uint8_t* box0 = my_out + (n_out & 1) * (2 * kOutBoxBf16Bytes);
@@ -801,6 +828,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             bulk_commit();
           }
           ++n_out;
+          // the input box just read is free again: refill it kInDepth blocks ahead
+          // (the lanes' reads of it precede the fence and the warp barrier above)
+          if (prefetch_in && (c0 >> 5) + kInDepth < n_blocks)
+            request_in(n0 + c0 + 32 * kInDepth, m0 + quarter * 32, hb, sb);
         }
       }
       tc_fence_before();

@@ -225,7 +225,7 @@ def mlp_set_split_tail(enable: bool):
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
                3: "B3 gemm Y_i^T.dZ (+= dB)", 4: "B4 gemm X^T.dU_i (+= dA)", 5: "B5 gemm dU_i.A_i^T (+dO)",
                10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset", 14: "adam step",
-               20: "attention GEMM", 21: "softmax fwd/bwd"}
+               20: "attention GEMM", 21: "softmax, softmax-grad row sums"}
 GEMM_KINDS = (0, 1, 2, 3, 4, 5)
 
 
