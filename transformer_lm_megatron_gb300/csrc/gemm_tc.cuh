@@ -710,8 +710,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           for (int q = 0; q < n_first; ++q) wait_in(n_in_used++);
         }
       }
-#pragma unroll 1
-      for (int c0 = 0; c0 < (finisher ? kBN : 0); c0 += 32) {
+      // One column block (32 columns) of this warp's rows: r holds its accumulator.
+      auto pace_block = [&](int c0) {
         if (ep.pace && nkb_next > 0 && c0 > 0) {
           // Pace the output: column block c0 / 32 (of 8) leaves once the producer is
           // about (3 / 32) * (c0 / 32) of the way through the next tile's copies, so
@@ -726,9 +726,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           __syncwarp();
         }
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c0, r);
-        tmem_ld_wait();
+      };
+      auto out_block = [&](int c0, uint32_t (&r)[32]) {
         if (other != nullptr) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
@@ -833,6 +832,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (prefetch_in && (c0 >> 5) + kInDepth < n_blocks)
             request_in(n0 + c0 + 32 * kInDepth, m0 + quarter * 32, hb, sb);
         }
+      };
+#pragma unroll 1
+      for (int c0 = 0; c0 < (finisher ? kBN : 0); c0 += 32) {
+        pace_block(c0);
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c0, r);
+        tmem_ld_wait();
+        out_block(c0, r);
       }
       tc_fence_before();
       __syncwarp();
