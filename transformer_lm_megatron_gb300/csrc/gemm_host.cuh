@@ -91,7 +91,7 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
                   const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
                   int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind, int batch = 1,
                   int nb_h = 1, int causal = kCausalNone, bool late_wait = false) {
-  using Cfg = GemmCfg<PAIR>;
+  using Cfg = GemmCfg<PAIR, BATCHED>;
   auto kern = k_gemm_bf16_tc<AM, BM, PAIR, BATCHED>;
   const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0) + (BATCHED ? 8 : 0);
   if (!st->gemm_attr[slot]) {
@@ -101,7 +101,7 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
       cudaLaunchConfig_t qc = {};
       qc.gridDim = dim3(2 * (unsigned)st->sms, 1, 1);
-      qc.blockDim = dim3(kGemmThreads, 1, 1);
+      qc.blockDim = dim3(Cfg::kThreads, 1, 1);
       qc.dynamicSmemBytes = Cfg::kSmemBytes;
       cudaLaunchAttribute qa[1];
       qa[0].id = cudaLaunchAttributeClusterDimension;
@@ -151,12 +151,12 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
   cudaError_t e;
   if (PAIR) {
     const int pairs = (int)(items < st->max_pairs[slot] ? items : st->max_pairs[slot]);
-    e = launch_kernel(kern, dim3(2 * (unsigned)pairs), dim3(kGemmThreads), Cfg::kSmemBytes, stream, 2, 1, mA, mB, mC,
+    e = launch_kernel(kern, dim3(2 * (unsigned)pairs), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, 2, 1, mA, mB, mC,
                       mO0, mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
                       st->status);
   } else {
     const int grid = (int)(items < st->sms ? items : st->sms);
-    e = launch_kernel(kern, dim3((unsigned)grid), dim3(kGemmThreads), Cfg::kSmemBytes, stream, 1, 1, mA, mB, mC, mO0,
+    e = launch_kernel(kern, dim3((unsigned)grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, 1, 1, mA, mB, mC, mO0,
                       mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
                       st->status);
   }

@@ -13,14 +13,15 @@
 //               its own 128 rows of A and its half (128) of B's columns, so per
 //               SM the B traffic (smem and L2) halves; 6-stage ring of 32 KB.
 //
-// Warp roles (192 threads, one CTA per SM):
+// Warp roles (192 threads, or 320 for batched GEMMs; one CTA per SM):
 //   warp 0      TMA producer: loads A/B k-blocks into the smem ring.
 //   warp 1      TMEM owner and (even CTA) MMA issuer: one thread issues
 //               tcgen05.mma; the accumulator is double-buffered (2 x 256 fp32
 //               columns of TMEM) so the epilogue of tile j overlaps the main
 //               loop of tile j+1.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lane
-//               quarter w % 4, i.e. tile rows 32*(w%4) .. +31), fused element-wise
+//               quarter w % 4, i.e. tile rows 32*(w%4) .. +31; batched GEMMs have
+//               warps 2..9, two per quarter, each on half the columns), fused element-wise
 //               work, TMA stores.  The 8 column blocks of a tile leave paced
 //               against the producer's progress through the next tile: a burst
 //               of output stores (fp32 gradients above all) starves that tile's
@@ -39,7 +40,6 @@ namespace gbmlp {
 constexpr int kBM = 128;   // rows of D per CTA per tile
 constexpr int kBN = 256;   // columns of D per tile (the MMA's N)
 constexpr int kBK = 64;
-constexpr int kGemmThreads = 192;
 constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kChunkBytes = 64 * kBK * 2;  // one 64 x BK box of an MN-major operand
 constexpr uint32_t kTmemCols = 2 * kBN;         // double-buffered accumulator
@@ -50,23 +50,30 @@ constexpr uint32_t kTmemCols = 2 * kBN;         // double-buffered accumulator
 // per buffer for the GeLU epilogue, which writes U and Y).
 constexpr uint32_t kOutBoxBytes = 32 * 32 * 4;
 constexpr uint32_t kOutBoxBf16Bytes = 32 * 32 * 2;
-constexpr uint32_t kOutStageBytes = 4 * 2 * kOutBoxBytes;  // 4 warps x 2 buffers
 // Longest an epilogue warp waits for the main loop before it stores anyway.
 constexpr uint64_t kPaceLimitNs = 200000;
 
 // Staged epilogue inputs (see the epilogue) live in the free halves of the two
 // output buffers of each epilogue warp: a ring of kInDepth = 2 boxes.
-template <bool PAIR>
+// Batched GEMMs (the attention products: reductions over a head size, so their
+// time is in the epilogue) run 8 epilogue warps, two per TMEM lane quarter, each
+// on half of the tile's columns, and pay for the extra staging with a shorter ring.
+template <bool PAIR, bool BATCHED = false>
 struct GemmCfg {
-  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kEpiWarps = BATCHED ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kStages = BATCHED ? (PAIR ? 5 : 3) : (PAIR ? 6 : 4);
   static constexpr int kBLoadN = PAIR ? kBN / 2 : kBN;      // B rows (N) this CTA loads per stage
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;       // rows of D per tile
   static constexpr uint32_t kBBytes = kBLoadN * kBK * 2;
   static constexpr uint32_t kStageBytes = kABytes + kBBytes;
   static constexpr int kInDepth = 2;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kOutStageBytes + 1024 /*align*/ + 256;
+  static constexpr uint32_t kOutBytes = kEpiWarps * 2 * kOutBoxBytes;  // 2 staging buffers per epilogue warp
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + kOutBytes + 1024 /*align*/ + 512 /*barriers*/;
 };
-static_assert(GemmCfg<true>::kSmemBytes <= 232448 && GemmCfg<false>::kSmemBytes <= 232448, "smem budget");
+static_assert(GemmCfg<true>::kSmemBytes <= 232448 && GemmCfg<false>::kSmemBytes <= 232448 &&
+                  GemmCfg<true, true>::kSmemBytes <= 232448 && GemmCfg<false, true>::kSmemBytes <= 232448,
+              "smem budget");
 
 enum CausalMode : int { kCausalNone = 0, kCausalSkipUpper = 1, kCausalKUpTo = 2, kCausalKFrom = 3 };
 
@@ -277,20 +284,21 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // each tile's reduction after its last row (A(m, k) = 0 for k > m);
 // kCausalKFrom starts it at the tile's first row (A(m, k) = 0 for k < m).
 template <bool A_MN, bool B_MN, bool PAIR, bool BATCHED>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED>::kThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
                    int group, int l2_hints, int batch, int nb_h, int causal, int late_wait, int* status) {
-  using Cfg = GemmCfg<PAIR>;
+  using Cfg = GemmCfg<PAIR, BATCHED>;
   constexpr int kStages = Cfg::kStages;
+  constexpr int kEpiWarps = Cfg::kEpiWarps;
   constexpr int kInDepth = Cfg::kInDepth;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
   uint8_t* sOut = sB + kStages * Cfg::kBBytes;  // 1024-aligned
-  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + kOutStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + Cfg::kOutBytes);
   uint64_t* empty = full + kStages;
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 2;
@@ -323,10 +331,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
+      mbar_init(&acc_empty[a], (PAIR ? 2 : 1) * kEpiWarps);  // one arrival per epilogue warp (of both CTAs)
     }
     mbar_init(mma_done, 1);
-    for (int i = 0; i < 4 * kInDepth; ++i) mbar_init(&in_full[i], 1);
+    for (int i = 0; i < kEpiWarps * kInDepth; ++i) mbar_init(&in_full[i], 1);
     fence_mbar_init();
   }
   const bool tma_out = epi_f32_out(ep.kind);
@@ -621,6 +629,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // -------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
+    // this warp's columns of each tile: all 256, or one half (8 epilogue warps)
+    const int col_begin = kEpiWarps == 8 ? ((warp - 2) >> 2) * (kBN / 2) : 0;
+    const int col_end = col_begin + kBN * 4 / kEpiWarps;
     uint8_t* my_out = sOut + (warp - 2) * 2 * kOutBoxBytes;
     uint32_t n_out = 0;  // boxes this warp has issued
     const int hout = (l2_hints >> 4) & 3;
@@ -666,10 +677,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
       // column blocks of this warp that produce output (the rest are clipped)
       const bool rows_in = m0 + quarter * 32 < M;
-      const int n_blocks = (prefetch_in && rows_in && n0 < N) ? min(kBN / 32, (N - n0 + 31) / 32) : 0;
+      const int n_blocks = (prefetch_in && rows_in && n0 + col_begin < N)
+                               ? min((col_end - col_begin) / 32, (N - n0 - col_begin + 31) / 32) : 0;
       uint32_t n_in_used = n_in;  // index of the next input box to consume
       const int n_first = min(n_blocks, kInDepth);
-      for (int q = 0; q < n_first; ++q) request_in(n0 + 32 * q, m0 + quarter * 32, hb, sb);
+      for (int q = 0; q < n_first; ++q) request_in(n0 + col_begin + 32 * q, m0 + quarter * 32, hb, sb);
       if (!(PAIR ? mbar_wait_cluster(&acc_full[acc], acc_phase) : mbar_wait(&acc_full[acc], acc_phase))) {
         record_status(status, kStatusTimeout, 6);
         break;
@@ -829,12 +841,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ++n_out;
           // the input box just read is free again: refill it kInDepth blocks ahead
           // (the lanes' reads of it precede the fence and the warp barrier above)
-          if (prefetch_in && (c0 >> 5) + kInDepth < n_blocks)
+          if (prefetch_in && ((c0 - col_begin) >> 5) + kInDepth < n_blocks)
             request_in(n0 + c0 + 32 * kInDepth, m0 + quarter * 32, hb, sb);
         }
       };
 #pragma unroll 1
-      for (int c0 = 0; c0 < (finisher ? kBN : 0); c0 += 32) {
+      for (int c0 = col_begin; c0 < (finisher ? col_end : col_begin); c0 += 32) {
         pace_block(c0);
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_row + c0, r);
