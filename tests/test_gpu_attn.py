@@ -40,6 +40,14 @@ def _weights(h, gen, std=0.02):
     return rnd(h, 3 * h), rnd(3 * h), rnd(h, h), rnd(h)
 
 
+@pytest.fixture
+def cta_pair_mode(request):
+    mlp.mlp_set_cta_pair(request.param)
+    yield request.param
+    mlp.mlp_set_cta_pair(-1)
+
+
+@pytest.mark.parametrize("cta_pair_mode", [0, 1], indirect=True, ids=["single", "pair"])
 @pytest.mark.parametrize("T,h,nh,t,L,k", [
     (256, 256, 4, 2, 128, 2),     # two sequences, d = 64, two accumulated micro-batches
     (272, 320, 4, 4, 136, 1),     # ragged: d = 80, seq_len 136 (tails in every GEMM)
@@ -47,7 +55,7 @@ def _weights(h, gen, std=0.02):
     (2048, 256, 2, 2, 2048, 1),    # one sequence of 2048: the longest rows the warp-per-row softmax holds
     (2304, 128, 2, 1, 2304, 1),    # rows past 2048 columns: the CTA-per-row softmax
 ])
-def test_attention_block_full_parity(T, h, nh, t, L, k):
+def test_attention_block_full_parity(T, h, nh, t, L, k, cta_pair_mode):
     p, seed = 0.1, 1234
     gen = torch.Generator().manual_seed(21)
     w = _weights(h, gen, std=0.5 / np.sqrt(h))
