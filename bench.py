@@ -46,11 +46,24 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_mtnlg_dram.md")
 GEMM_SOURCES = ["gemm_tc.cuh", "ptx.cuh", "block_math.cuh", "gemm_host.cuh"]
 
 
+def gemm_source_hash() -> str:
+    """sha256 of the GEMM sources with // comments and blank lines removed, so that
+    an edit of comments alone keeps a capture valid and any code change voids it."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "transformer_lm_megatron_gb300", "csrc", name)) as fh:
+            for line in fh:
+                code = line.split("//", 1)[0].rstrip()
+                if code:
+                    h.update((code + "\n").encode())
+    return h.hexdigest()
+
+
 def gemm_traffic_per_launch(workload: str):
     """DRAM bytes (read + write) per GEMM launch from the committed ncu capture of
-    the MT-NLG layer, or None if the workload differs or the GEMM sources changed
-    since the capture (the file records a hash of them)."""
-    import hashlib
+    the MT-NLG layer, or None if the workload differs or the GEMM code changed
+    since the capture (the file records gemm_source_hash() of it)."""
     if workload != "mtnlg" or not os.path.exists(TRAFFIC_PROFILE):
         return None
     fields = {}
@@ -59,11 +72,7 @@ def gemm_traffic_per_launch(workload: str):
             if ":" in line and line.split(":")[0] in ("bytes_per_launch_avg", "source_sha256"):
                 k, v = line.split(":", 1)
                 fields[k] = v.strip()
-    h = hashlib.sha256()
-    for name in GEMM_SOURCES:
-        with open(os.path.join(ROOT, "transformer_lm_megatron_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
-    if fields.get("source_sha256") != h.hexdigest() or "bytes_per_launch_avg" not in fields:
+    if fields.get("source_sha256") != gemm_source_hash() or "bytes_per_launch_avg" not in fields:
         return None
     return float(fields["bytes_per_launch_avg"])
 

@@ -12,6 +12,10 @@
 //               tcgen05.mma.cta_group::2 issued by the even CTA: each CTA loads
 //               its own 128 rows of A and its half (128) of B's columns, so per
 //               SM the B traffic (smem and L2) halves; 6-stage ring of 32 KB.
+// (Batched GEMMs: 3 and 5 stages, see GemmCfg.)  The grid is persistent: CTAs
+// (pairs) take work items round-robin; an item is a tile, or, in the split tail
+// of a GEMM whose last wave would be at most half full, one half of a tile's
+// reduction (see EpiParams).
 //
 // Warp roles (192 threads, or 320 for batched GEMMs; one CTA per SM):
 //   warp 0      TMA producer: loads A/B k-blocks into the smem ring.
