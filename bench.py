@@ -60,6 +60,14 @@ def gemm_source_hash() -> str:
     return h.hexdigest()
 
 
+def step_time_summary(step_ms):
+    """Median, min and max of per-step times (ms)."""
+    v = sorted(step_ms)
+    n = len(v)
+    med = v[n // 2] if n % 2 else 0.5 * (v[n // 2 - 1] + v[n // 2])
+    return {"median": med, "min": v[0], "max": v[-1]}
+
+
 def gemm_traffic_per_launch(workload: str):
     """DRAM bytes (read + write) per GEMM launch from the committed ncu capture of
     the MT-NLG layer, or None if the workload differs or the GEMM code changed
@@ -444,13 +452,18 @@ def run_ours(args, wl, rank, world, dist):
     ev1 = torch.cuda.Event(enable_timing=True)
     if trace:
         trace.start()
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps - 1)]
     ev0.record(stream)
-    for _ in range(args.steps):
+    for i in range(args.steps):
         step()
+        if i < args.steps - 1:
+            step_ev[i].record(stream)  # step boundaries, for the per-step spread
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     if trace:
         trace.stop()
+    bounds = [ev0] + step_ev + [ev1]
+    step_ms = [bounds[i].elapsed_time(bounds[i + 1]) for i in range(args.steps)]
     n_launch = mlp.mlp_launch_count() - n_launch0
     if dist is not None:
         dist.barrier()
@@ -621,7 +634,8 @@ def run_ours(args, wl, rank, world, dist):
     burst = peaks["bf16_burst"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "step_ms": step_time_summary(step_ms), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "pct_of_peak": 100.0 * value / (world * burst),
         "peak_tflops": {"value": burst, "kind": f"bf16 dense burst, {peaks['source']}"},

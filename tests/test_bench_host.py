@@ -60,3 +60,25 @@ def test_traffic_figure_tracks_the_gemm_sources():
     value = bench.gemm_traffic_per_launch("mtnlg")
     assert value is None or value > 0
     assert bench.gemm_traffic_per_launch("tiny") is None
+
+
+def test_gemm_hash_ignores_comments_only(tmp_path, monkeypatch):
+    """The capture key changes with the GEMM code, not with its comments."""
+    import shutil
+    csrc = tmp_path / "transformer_lm_megatron_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for name in bench.GEMM_SOURCES:
+        shutil.copy(os.path.join(bench.ROOT, "transformer_lm_megatron_gb300", "csrc", name), csrc / name)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h0 = bench.gemm_source_hash()
+    with open(csrc / "gemm_tc.cuh", "a") as fh:
+        fh.write("\n// a comment\n\n")
+    assert bench.gemm_source_hash() == h0
+    with open(csrc / "gemm_tc.cuh", "a") as fh:
+        fh.write("constexpr int kNotThere = 1;\n")
+    assert bench.gemm_source_hash() != h0
+
+
+def test_step_time_summary():
+    s = bench.step_time_summary([3.0, 1.0, 2.0, 10.0])
+    assert s == {"median": 2.5, "min": 1.0, "max": 10.0}
