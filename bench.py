@@ -620,10 +620,10 @@ def run_ours(args, wl, rank, world, dist):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         w_host = tuple(x.cpu() for x in weights)
-        dt, fl = oracle_sample(wl, oracle_sample_inputs(wl, w_host, args.cpu_tokens))
+        dt, fl = oracle_sample(wl, oracle_sample_inputs(wl, w_host, args.cpu_baseline_tokens))
         del w_host
         cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(), "kind": "oracle",
-               "sample": f"{args.cpu_tokens} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, "
+               "sample": f"{args.cpu_baseline_tokens} of {wl.tokens} tokens x slice 0 of {wl.t} (f={wl.f}), fwd+bwd, "
                          f"float64 numpy, {dt:.1f} s"}
         cpu["parity"] = sampled_parity(wl, weights, mbs[0][0], mbs[0][1], buf, stream)
     if adam is not None:
@@ -665,7 +665,10 @@ def main():
     ap.add_argument("--workload", default="mtnlg")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--slice-mode", default="all", choices=["all", "each"])
-    ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--cpu-tokens", type=int, default=32,
+                    help="tokens of the oracle sample per step of the reference arm")
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=512,
+                    help="tokens of the timed oracle sample of this arm's cpu_baseline (about 10 s of CPU work)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", dest="trace", action="store_false")
