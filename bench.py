@@ -667,8 +667,9 @@ def main():
     ap.add_argument("--slice-mode", default="all", choices=["all", "each"])
     ap.add_argument("--cpu-tokens", type=int, default=32,
                     help="tokens of the oracle sample per step of the reference arm")
-    ap.add_argument("--cpu-baseline-tokens", type=int, default=512,
-                    help="tokens of the timed oracle sample of this arm's cpu_baseline (about 10 s of CPU work)")
+    ap.add_argument("--cpu-baseline-tokens", type=int, default=2048,
+                    help="tokens of the timed oracle sample of this arm's cpu_baseline (10-15 s of CPU work on "
+                         "16 cores for the MT-NLG layer's slice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-trace", dest="trace", action="store_false")
