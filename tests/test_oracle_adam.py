@@ -55,3 +55,31 @@ def test_zero_gradient_only_decays():
     np.testing.assert_array_equal(m, 0.0)
     np.testing.assert_array_equal(v, 0.0)
     np.testing.assert_allclose(w, master * (1 - 1e-4), rtol=1e-15)
+
+
+def test_planted_mistakes_are_caught():
+    """No bias correction, eps inside the square root, or weight decay coupled into
+    the gradient (L2 instead of decoupled) all break the AdamW pin."""
+    rng = np.random.default_rng(5)
+    n = 2048
+    grad, master, m, v = _state(n, rng)
+    lr, b1, b2, eps, wd, step = 1e-3, 0.9, 0.95, 1e-8, 0.1, 3
+    p = torch.nn.Parameter(torch.from_numpy(master.copy()))
+    opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd)
+    opt.state[p] = {"step": torch.tensor(float(step - 1)), "exp_avg": torch.from_numpy(m.copy()),
+                    "exp_avg_sq": torch.from_numpy(v.copy())}
+    p.grad = torch.from_numpy(grad.copy())
+    opt.step()
+    ref = p.detach().numpy()
+    w, _, _, _ = ado.adam_step(grad, master, m, v, step, lr, b1, b2, eps, wd)
+    np.testing.assert_allclose(w, ref, rtol=1e-12, atol=1e-15)
+    m1 = b1 * m + (1 - b1) * grad
+    v1 = b2 * v + (1 - b2) * grad * grad
+    no_bias_corr = master - lr * wd * master - lr * m1 / (np.sqrt(v1) + eps)
+    eps_inside = master - lr * wd * master - (lr / (1 - b1 ** step)) * m1 / np.sqrt(v1 / (1 - b2 ** step) + eps)
+    g2 = grad + wd * master
+    m2 = b1 * m + (1 - b1) * g2
+    v2 = b2 * v + (1 - b2) * g2 * g2
+    coupled = master - (lr / (1 - b1 ** step)) * m2 / (np.sqrt(v2 / (1 - b2 ** step)) + eps)
+    for bad in (no_bias_corr, eps_inside, coupled):
+        assert not np.allclose(bad, ref, rtol=1e-12, atol=1e-15)  # the pin's tolerance

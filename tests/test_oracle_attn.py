@@ -98,3 +98,48 @@ def test_mirror_mode_rounds_at_storage_points():
     bm = ato.attn_bwd(dOut, X, Wqkv, Wo, fm["QKV"], fm["P"], fm["O"], fm["keep"], 4, 2, 8, 0.1, mirror=True)
     for arr in (fm["QKV"], fm["P"], fm["O"], fm["out"], bm["dZ"], bm["dO"], bm["dQKV"], bm["dX"]):
         np.testing.assert_array_equal(orc.round_bf16(arr), arr)
+
+
+def test_planted_mistakes_are_caught():
+    """A dropped 1/sqrt(d), a causal mask one key too wide, a sign error in the
+    softmax gradient or Q/K taken from the wrong block all break the torch pin."""
+    rng = np.random.default_rng(23)
+    T, h, nh, t, L, p, seed = 16, 8, 2, 1, 8, 0.2, 3
+    X, Wqkv, bqkv, Wo, bo, dOut = _inputs(T, h, rng, std=0.5)
+    fw = ato.attn_fwd(X, Wqkv, bqkv, Wo, bo, nh, t, L, p, seed)
+    ref = _torch_block(X, Wqkv, bqkv, Wo, bo, fw["keep"], p, dOut, nh, L)
+    d = h // nh
+    QKV = fw["QKV"]
+
+    def head_out(scale, wide, q_block=0, k_block=1):
+        O = np.zeros((T, h))
+        for s in range(T // L):
+            rows = slice(s * L, (s + 1) * L)
+            for j in range(nh):
+                q = QKV[rows, q_block * h + j * d:q_block * h + (j + 1) * d]
+                k = QKV[rows, k_block * h + j * d:k_block * h + (j + 1) * d]
+                v = QKV[rows, 2 * h + j * d:2 * h + (j + 1) * d]
+                mask = np.tril(np.ones((L, L), dtype=bool), k=1 if wide else 0)
+                sc = np.where(mask, (q @ k.T) * scale, -np.inf)
+                e = np.exp(sc - sc.max(axis=1, keepdims=True))
+                O[rows, j * d:(j + 1) * d] = (e / e.sum(axis=1, keepdims=True)) @ v
+        return O
+
+    np.testing.assert_allclose(head_out(1 / np.sqrt(d), False), ref["O"], rtol=1e-10, atol=1e-12)
+    assert np.max(np.abs(head_out(1.0, False) - ref["O"])) > 1e-6             # dropped 1/sqrt(d)
+    assert np.max(np.abs(head_out(1 / np.sqrt(d), True) - ref["O"])) > 1e-6   # mask one key too wide
+    assert np.max(np.abs(head_out(1 / np.sqrt(d), False, 1, 0) - ref["O"])) > 1e-6  # Q and K swapped
+    # softmax gradient with the sign of the row sum flipped
+    bw = ato.attn_bwd(dOut, X, Wqkv, Wo, QKV, fw["P"], fw["O"], fw["keep"], nh, t, L, p)
+    np.testing.assert_allclose(bw["dWqkv"], ref["dWqkv"], rtol=1e-10, atol=1e-11)
+    dQ = np.zeros((T, h))
+    for s in range(T // L):
+        rows = slice(s * L, (s + 1) * L)
+        for j in range(nh):
+            pr = fw["P"][s, j]
+            do = bw["dO"][rows, j * d:(j + 1) * d]
+            dp = do @ QKV[rows, 2 * h + j * d:2 * h + (j + 1) * d].T
+            ds = pr * (dp + (dp * pr).sum(axis=1, keepdims=True)) / np.sqrt(d)
+            dQ[rows, j * d:(j + 1) * d] = ds @ QKV[rows, h + j * d:h + (j + 1) * d]
+    bad_dWq = X.T @ dQ
+    assert np.max(np.abs(bad_dWq - ref["dWqkv"][:, :h])) > 1e-6
