@@ -109,3 +109,37 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(8, 8)
     with pytest.raises(ValueError):
         mlp._ptr(x) if not torch.cuda.is_available() else (_ for _ in ()).throw(ValueError())
+
+
+def test_switches_reject_bad_values(lib):
+    assert lib.mlp_set_cta_pair(2) == mlp.MLP_EINVAL
+    assert lib.mlp_set_dependent_launch(2) == mlp.MLP_EINVAL
+    assert lib.mlp_set_split_tail(-1) == mlp.MLP_EINVAL
+    for fn in (lib.mlp_set_cta_pair, lib.mlp_set_dependent_launch, lib.mlp_set_split_tail):
+        assert fn(1) == mlp.MLP_OK
+    assert lib.mlp_set_cta_pair(-1) == mlp.MLP_OK
+
+
+def test_adam_rejects_bad_arguments(lib):
+    def call(**kw):
+        a = dict(n=1024, grad=GOOD, grad_scale=1.0, master=GOOD, m=GOOD, v=GOOD, weight=GOOD, lr=1e-3, beta1=0.9,
+                 beta2=0.95, eps=1e-8, weight_decay=0.0, step=1)
+        a.update(kw)
+        return lib.adam_step(a["n"], a["grad"], a["grad_scale"], a["master"], a["m"], a["v"], a["weight"], a["lr"],
+                             a["beta1"], a["beta2"], a["eps"], a["weight_decay"], a["step"], None)
+    assert call(n=0) == mlp.MLP_EINVAL
+    assert call(step=0) == mlp.MLP_EINVAL
+    assert call(beta1=1.0) == mlp.MLP_EINVAL
+    assert call(eps=0.0) == mlp.MLP_EINVAL
+    assert call(m=None) == mlp.MLP_EINVAL
+    assert call(weight=GOOD + 2) == mlp.MLP_EALIGN
+
+
+def test_attention_rejects_bad_shapes_without_a_gpu(lib):
+    ptrs = [GOOD] * 5
+    outs = [GOOD] * 5
+    # h, nh, t, tokens, seq_len, p, seed, token_offset, X, Wqkv, bqkv, Wo, bo, R, QKV, S, P, O, out, stream
+    assert lib.attn_fwd(96, 16, 1, 64, 32, 0.1, 1, 0, *ptrs, None, *outs, None) == mlp.MLP_EINVAL   # d = 6
+    assert lib.attn_fwd(128, 4, 1, 60, 32, 0.1, 1, 0, *ptrs, None, *outs, None) == mlp.MLP_EINVAL   # 60 % 32
+    assert lib.attn_fwd(128, 4, 3, 64, 32, 0.1, 1, 0, *ptrs, None, *outs, None) == mlp.MLP_EINVAL   # t does not divide nh
+    assert lib.attn_fwd(128, 4, 1, 64, 32, 1.0, 1, 0, *ptrs, None, *outs, None) == mlp.MLP_EINVAL   # p = 1
