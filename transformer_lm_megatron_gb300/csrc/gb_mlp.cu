@@ -106,8 +106,8 @@ struct DeviceState {
   int* split_flags = nullptr;
   cudaStream_t split_owner[kSplitRegions] = {};  // the stream each region belongs to
   int split_regions_used = 0;
-  bool gemm_attr[16] = {};  // per GEMM instantiation: dynamic smem attribute set
-  int max_pairs[16] = {};   // per CTA-pair instantiation: co-resident clusters of two
+  bool gemm_attr[32] = {};  // per GEMM instantiation: dynamic smem attribute set
+  int max_pairs[32] = {};   // per CTA-pair instantiation: co-resident clusters of two
 };
 
 

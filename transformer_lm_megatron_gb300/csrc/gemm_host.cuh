@@ -86,14 +86,14 @@ int operand_map(CUtensorMap* m, const void* base, bool mn_major, int64_t mn, int
   return make_map(m, base, k, mn, ld, kBK, tile_mn);
 }
 
-template <bool AM, bool BM, bool PAIR, bool BATCHED = false>
+template <bool AM, bool BM, bool PAIR, bool BATCHED = false, bool WIDE = false>
 int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB, const CUtensorMap& mC,
                   const CUtensorMap& mO0, const CUtensorMap& mO1, int M, int N, int K, const EpiParams& ep,
                   int raster_n_fast, int group, int l2_hints, cudaStream_t stream, int trace_kind, int batch = 1,
                   int nb_h = 1, int causal = kCausalNone, bool late_wait = false) {
-  using Cfg = GemmCfg<PAIR, BATCHED>;
-  auto kern = k_gemm_bf16_tc<AM, BM, PAIR, BATCHED>;
-  const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0) + (BATCHED ? 8 : 0);
+  using Cfg = GemmCfg<PAIR, BATCHED || WIDE>;
+  auto kern = k_gemm_bf16_tc<AM, BM, PAIR, BATCHED, WIDE>;
+  const int slot = (AM ? 2 : 0) + (BM ? 1 : 0) + (PAIR ? 4 : 0) + (BATCHED ? 8 : 0) + (WIDE ? 16 : 0);
   if (!st->gemm_attr[slot]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::kSmemBytes);
     if (e != cudaSuccess) return fail(MLP_ECUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
@@ -135,7 +135,7 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
   epx.split_ws = nullptr;
   epx.split_flags = nullptr;
   int64_t items = tiles;
-  if (!BATCHED && causal == kCausalNone && !epi_f32_out(ep.kind) && !late_wait &&
+  if (!BATCHED && !WIDE && causal == kCausalNone && !epi_f32_out(ep.kind) && !late_wait &&
       g_split_tail.load(std::memory_order_relaxed) && (K + kBK - 1) / kBK >= 16) {
     const int64_t rem = tiles % units;
     const int region = (rem > 0 && 2 * rem <= units && rem * (PAIR ? 2 : 1) * 4 <= kSplitSlots)
@@ -215,21 +215,25 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
     if (group < 1) group = 1;
   }
   const int l2_hints = g_l2_hints.load(std::memory_order_relaxed);
-  if (!a_mn && b_mn)
-    return pair ? launch_gemm_t<false, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait)
-                : launch_gemm_t<false, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
-  if (!a_mn && !b_mn)
-    return pair ? launch_gemm_t<false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait)
-                : launch_gemm_t<false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
-  if (a_mn && b_mn)
-    return pair ? launch_gemm_t<true, true, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait)
-                : launch_gemm_t<true, true, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,
-                                                                group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
+  // Reductions under 16 k-blocks leave the time in the epilogue: 8 epilogue warps.
+  const bool wide = (K + kBK - 1) / kBK < 16;
+#define GB_LAUNCH(AM_, BM_)                                                                                        \
+  (pair ? (wide ? launch_gemm_t<AM_, BM_, true, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,   \
+                                                             group, l2_hints, stream, trace_kind, 1, 1, kCausalNone, \
+                                                             late_wait)                                              \
+                : launch_gemm_t<AM_, BM_, true, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,  \
+                                                              group, l2_hints, stream, trace_kind, 1, 1, kCausalNone,\
+                                                              late_wait))                                            \
+        : (wide ? launch_gemm_t<AM_, BM_, false, false, true>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast,  \
+                                                              group, l2_hints, stream, trace_kind, 1, 1, kCausalNone,\
+                                                              late_wait)                                             \
+                : launch_gemm_t<AM_, BM_, false, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, \
+                                                               group, l2_hints, stream, trace_kind, 1, 1,            \
+                                                               kCausalNone, late_wait)))
+  if (!a_mn && b_mn) return GB_LAUNCH(false, true);
+  if (!a_mn && !b_mn) return GB_LAUNCH(false, false);
+  if (a_mn && b_mn) return GB_LAUNCH(true, true);
+#undef GB_LAUNCH
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 

@@ -17,15 +17,16 @@
 // of a GEMM whose last wave would be at most half full, one half of a tile's
 // reduction (see EpiParams).
 //
-// Warp roles (192 threads, or 320 for batched GEMMs; one CTA per SM):
+// Warp roles (192 threads, or 320 in the wide configuration; one CTA per SM):
 //   warp 0      TMA producer: loads A/B k-blocks into the smem ring.
 //   warp 1      TMEM owner and (even CTA) MMA issuer: one thread issues
 //               tcgen05.mma; the accumulator is double-buffered (2 x 256 fp32
 //               columns of TMEM) so the epilogue of tile j overlaps the main
 //               loop of tile j+1.
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (warp w reads TMEM lane
-//               quarter w % 4, i.e. tile rows 32*(w%4) .. +31; batched GEMMs have
-//               warps 2..9, two per quarter, each on half the columns), fused element-wise
+//               quarter w % 4, i.e. tile rows 32*(w%4) .. +31; the wide
+//               configuration has warps 2..9, two per quarter, each on half the
+//               columns), fused element-wise
 //               work, TMA stores.  The 8 column blocks of a tile leave paced
 //               against the producer's progress through the next tile: a burst
 //               of output stores (fp32 gradients above all) starves that tile's
@@ -59,14 +60,15 @@ constexpr uint64_t kPaceLimitNs = 200000;
 
 // Staged epilogue inputs (see the epilogue) live in the free halves of the two
 // output buffers of each epilogue warp: a ring of kInDepth = 2 boxes.
-// Batched GEMMs (the attention products: reductions over a head size, so their
-// time is in the epilogue) run 8 epilogue warps, two per TMEM lane quarter, each
-// on half of the tile's columns, and pay for the extra staging with a shorter ring.
-template <bool PAIR, bool BATCHED = false>
+// WIDE configurations (the batched attention products, whose reductions run over
+// a head size, and plain GEMMs with reductions under 16 k-blocks: their time is in
+// the epilogue) run 8 epilogue warps, two per TMEM lane quarter, each on half of
+// the tile's columns, and pay for the extra staging with a shorter ring.
+template <bool PAIR, bool WIDE = false>
 struct GemmCfg {
-  static constexpr int kEpiWarps = BATCHED ? 8 : 4;
+  static constexpr int kEpiWarps = WIDE ? 8 : 4;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
-  static constexpr int kStages = BATCHED ? (PAIR ? 5 : 3) : (PAIR ? 6 : 4);
+  static constexpr int kStages = WIDE ? (PAIR ? 5 : 3) : (PAIR ? 6 : 4);
   static constexpr int kBLoadN = PAIR ? kBN / 2 : kBN;      // B rows (N) this CTA loads per stage
   static constexpr int kTileM = PAIR ? 2 * kBM : kBM;       // rows of D per tile
   static constexpr uint32_t kBBytes = kBLoadN * kBK * 2;
@@ -287,13 +289,13 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // after the tile's last row (the result there is never read); kCausalKUpTo stops
 // each tile's reduction after its last row (A(m, k) = 0 for k > m);
 // kCausalKFrom starts it at the tile's first row (A(m, k) = 0 for k < m).
-template <bool A_MN, bool B_MN, bool PAIR, bool BATCHED>
-__global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED>::kThreads, 1)
+template <bool A_MN, bool B_MN, bool PAIR, bool BATCHED, bool WIDE = false>
+__global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
                    int group, int l2_hints, int batch, int nb_h, int causal, int late_wait, int* status) {
-  using Cfg = GemmCfg<PAIR, BATCHED>;
+  using Cfg = GemmCfg<PAIR, BATCHED || WIDE>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kEpiWarps = Cfg::kEpiWarps;
   constexpr int kInDepth = Cfg::kInDepth;
@@ -382,7 +384,8 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED>::kThreads, 1)
   }
   // Work items: tiles [0, split_base) whole, then each tile of the split tail as two
   // items, one per half of its reduction (see EpiParams).
-  const int split_base = (!BATCHED && ep.split_ws != nullptr) ? min(ep.split_base, num_tiles) : num_tiles;
+  const int split_base =
+      (!BATCHED && kEpiWarps == 4 && ep.split_ws != nullptr) ? min(ep.split_base, num_tiles) : num_tiles;
   const int num_items = split_base + 2 * (num_tiles - split_base);
   const int item_end = skip ? 0 : num_items;
 
