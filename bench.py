@@ -42,8 +42,11 @@ def _peaks():
 
 
 # ----------------------------------------------------------------------------- ncu traffic
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_tc_mtnlg_dram.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "gemm_tc_dram_traffic.json")
 GEMM_SOURCES = ["gemm_tc.cuh", "ptx.cuh", "block_math.cuh", "gemm_host.cuh"]
+# Sustained peak only for timed regions at least this long (seconds); shorter
+# regions run at the burst rate the driver measured with a 10-iteration matmul.
+SUSTAINED_MIN_S = 3.0
 
 
 def gemm_source_hash() -> str:
@@ -60,29 +63,30 @@ def gemm_source_hash() -> str:
     return h.hexdigest()
 
 
+def gemm_traffic_per_launch(workload: str):
+    """DRAM bytes (read + write) per GEMM launch of ``workload``, scaled from the
+    committed ncu record (profiles/gemm_tc_dram_traffic.json: a capture of the six
+    GEMM launches of one slice-sized block, scaled to a full launch by the units
+    each processes), or None if there is no record for the workload or the GEMM
+    code changed since it was taken (the record holds gemm_source_hash())."""
+    if not os.path.exists(TRAFFIC_RECORD):
+        return None
+    with open(TRAFFIC_RECORD) as fh:
+        rec = json.load(fh)
+    if rec.get("source_sha256") != gemm_source_hash():
+        return None
+    full = rec.get("scaled_to", {}).get(workload)
+    if not full:
+        return None
+    return float(full["bytes_per_launch_avg"])
+
+
 def step_time_summary(step_ms):
     """Median, min and max of per-step times (ms)."""
     v = sorted(step_ms)
     n = len(v)
     med = v[n // 2] if n % 2 else 0.5 * (v[n // 2 - 1] + v[n // 2])
     return {"median": med, "min": v[0], "max": v[-1]}
-
-
-def gemm_traffic_per_launch(workload: str):
-    """DRAM bytes (read + write) per GEMM launch from the committed ncu capture of
-    the MT-NLG layer, or None if the workload differs or the GEMM code changed
-    since the capture (the file records gemm_source_hash() of it)."""
-    if workload != "mtnlg" or not os.path.exists(TRAFFIC_PROFILE):
-        return None
-    fields = {}
-    with open(TRAFFIC_PROFILE) as fh:
-        for line in fh:
-            if ":" in line and line.split(":")[0] in ("bytes_per_launch_avg", "source_sha256"):
-                k, v = line.split(":", 1)
-                fields[k] = v.strip()
-    if fields.get("source_sha256") != gemm_source_hash() or "bytes_per_launch_avg" not in fields:
-        return None
-    return float(fields["bytes_per_launch_avg"])
 
 
 def hbm_kernel_rooflines(trace, wl, peaks, reset_ms):
@@ -279,7 +283,6 @@ def other_workloads(dev, stream, steps=5, warmup=2):
     return out
 
 
-ATTN_SHAPE = dict(h=20480, nh=128, t=8, seq_len=2048, tokens=2048)
 
 
 def attn_flops(tokens, h, seq_len):
@@ -293,15 +296,10 @@ def attn_flops(tokens, h, seq_len):
 def attn_bench(wl, dev, stream, args):
     import torch
     from transformer_lm_megatron_gb300 import mlp
-    c = ATTN_SHAPE
+    from transformer_lm_megatron_gb300 import inputs as gin
+    c = gin.ATTN_MTNLG
     h, nh, t, L, T = c["h"], c["nh"], c["t"], c["seq_len"], c["tokens"]
-    g = torch.Generator(device=dev).manual_seed(7)
-
-    def rnd(*shape, std):
-        return (torch.randn(*shape, generator=g, device=dev) * std).to(torch.bfloat16)
-
-    w = (rnd(h, 3 * h, std=0.02), rnd(3 * h, std=0.02), rnd(h, h, std=0.02), rnd(h, std=0.02))
-    X, dOut = rnd(T, h, std=1.0), rnd(T, h, std=1.0)
+    w, X, dOut = gin.make_attn_inputs(h, T, device=dev)
     buf = mlp.AttnBuffers(T, h, nh, L, device=dev)
 
     def step():
@@ -465,6 +463,40 @@ def run_ours(args, wl, rank, world, dist):
     bounds = [ev0] + step_ev + [ev1]
     step_ms = [bounds[i].elapsed_time(bounds[i + 1]) for i in range(args.steps)]
     n_launch = mlp.mlp_launch_count() - n_launch0
+
+    # ---- the += form of the same step, inside the same clock record: the
+    # accumulators are zeroed by grad_accum_reset OUTSIDE the event-timed region,
+    # then every micro-batch adds its gradients (fp32 reduce-add epilogues).
+    acc_form = None
+    if not args.no_accumulate_form:
+        def acc_step():
+            for j, (X, dO) in enumerate(mbs):
+                mlp.block_step(wl, weights, X, dO, buf, token_offset=j * wl.tokens, slice_mode=args.slice_mode,
+                               stream=stream, accumulate=True)
+        for _ in range(2):
+            reset()
+            acc_step()
+        torch.cuda.synchronize(dev)
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                 for _ in range(2 * args.steps)]
+        for i in range(args.steps):
+            r0, r1 = pairs[2 * i]
+            a0, a1 = pairs[2 * i + 1]
+            r0.record(stream)
+            reset()
+            r1.record(stream)
+            a0.record(stream)
+            acc_step()
+            a1.record(stream)
+        torch.cuda.synchronize(dev)
+        acc_ms = max_over_ranks(sum(pairs[2 * i + 1][0].elapsed_time(pairs[2 * i + 1][1]) for i in range(args.steps)),
+                                dist, dev)
+        reset_ms_total = sum(pairs[2 * i][0].elapsed_time(pairs[2 * i][1]) for i in range(args.steps))
+        acc_form = {"value": job_throughput(wl.flops_total(), args.steps, world, acc_ms), "unit": UNIT,
+                    "ms_per_step": acc_ms / args.steps, "reset_ms_per_step": reset_ms_total / args.steps,
+                    "grad_init": "grad_accum_reset before each step, outside the timed events; every micro-batch "
+                                 "adds (+=) into dA, da, dB, db",
+                    "steps": args.steps}
     if dist is not None:
         dist.barrier()
     clock_info = clocks.stop() if clocks else None
@@ -611,11 +643,17 @@ def run_ours(args, wl, rank, world, dist):
     peaks = _peaks()
     roofline = None
     if trace:
-        roofline = trace.roofline(peaks, args.steps)
+        timed_s = ms / 1e3
+        if timed_s >= SUSTAINED_MIN_S:
+            peak, kind = peaks["bf16_sustained"], f"bf16 dense sustained ({peaks['source']}; timed region {timed_s:.2f} s)"
+        else:
+            peak, kind = peaks["bf16_burst"], f"bf16 dense burst ({peaks['source']}; timed region {timed_s:.2f} s)"
+        roofline = trace.roofline(peak, kind)
         if roofline is not None:
             roofline["hbm_kernels"] = hbm_kernel_rooflines(trace, wl, peaks, reset_ms)
             roofline["traffic"] = gemm_traffic_per_launch(wl.name)
-            roofline["traffic_unit"] = "bytes per GEMM launch (DRAM read + write, ncu)"
+            roofline["traffic_unit"] = ("bytes per GEMM launch (DRAM read + write; ncu capture of a slice-sized "
+                                        "block scaled to a full launch, profiles/gemm_tc_dram_traffic.json)")
             roofline["algorithmic_bytes_per_launch"] = 2 * (wl.tokens * wl.h + wl.h * wl.ffn + wl.tokens * wl.ffn)
     cpu = None
     if not args.no_cpu_baseline and world == 1:
@@ -650,6 +688,7 @@ def run_ours(args, wl, rank, world, dist):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "accumulate_form": acc_form,
         "clocks": clock_info,
         "other_workloads": others,
         "next_rows": {"adam_step": adam, "attn_block": attn},
@@ -676,6 +715,8 @@ def main():
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention-block measurement")
     ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-accumulate-form", action="store_true",
+                    help="skip timing the += form (reset outside the timed region, every micro-batch adds)")
     ap.add_argument("--reset-each-step", action="store_true",
                     help="time grad_accum_reset + all micro-batches adding, instead of the first writing")
     args = ap.parse_args()

@@ -31,8 +31,13 @@
  *     bfloat16.  Shapes: X, R, O, dO, dX, dZ [tokens, h]; U, Y, dU [tokens, ffn];
  *     A [h, ffn]; a [ffn]; B [ffn, h]; b [h]; dA [h, ffn]; da [ffn]; dB [ffn, h];
  *     db [h]; Zacc, dXacc [tokens, h] fp32.
- *   - All pointers are DEVICE pointers owned by the caller, 16-byte aligned.  The
- *     library allocates no device memory; it keeps only a 2-word status word.
+ *   - All pointers are DEVICE pointers owned by the caller, 16-byte aligned.  No
+ *     call allocates device memory.  The library's own device memory is static
+ *     module memory, held by every GPU that loads the library until the process
+ *     exits: the 2-word status word; the split-tail partial sums and arrival
+ *     counters of the GEMMs (4 regions of 304 x 2 x 32 x 256 fp32, about 20 MB
+ *     each, see mlp_set_split_tail); and the 16 MiB fp32 array of
+ *     mlp_fwd_static_scratch.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
  *     and runs asynchronously.  A nonzero return means nothing was enqueued,
  *     except MLP_ECUDA, which reports a failed launch (later launches of the same

@@ -123,3 +123,92 @@ def attn_bwd(dOut, X, Wqkv, Wo, QKV, P, O, keep, nh, t, seq_len, p, mirror=False
     dbqkv = dQKV.sum(axis=0)
     dX = _rb((dOut if residual_is_input else 0.0) + dQKV @ Wqkv.T, mirror)
     return {"dZ": dZ, "dO": dO, "dQKV": dQKV, "dX": dX, "dWqkv": dWqkv, "dbqkv": dbqkv, "dWo": dWo, "dbo": dbo}
+
+
+# ----------------------------------------------------------------------------
+# Sampled evaluation for shapes whose full float64 weight gradients do not fit in
+# host memory (the MT-NLG layer shape: dWqkv alone would be 10 GB).  The same
+# steps as attn_fwd / attn_bwd, in the same order and roundings; the weights are
+# read a column (or row) block at a time, so they may be given as
+# mlp_oracle.Bf16Matrix, and only the requested entries of the weight gradients
+# are formed.  Every token's Q, K, V and every head's attention are still
+# computed, because an output row of the block depends on all of them.
+# ----------------------------------------------------------------------------
+def attn_sampled(X, dOut, Wqkv, bqkv, Wo, bo, nh, t, seq_len, p, seed, rows, heads, wqkv_idx, wo_idx,
+                 token_offset=0, mirror=False, col_block=2560):
+    """Outputs of one forward + backward at sampled positions (residual R = X).
+
+    rows      token rows (global indices) of QKV, O, out, dQKV, dX, and of P
+    heads     heads whose probability rows P[seq(row), head, row, :] are returned
+    wqkv_idx  (r, c) index arrays of the dWqkv entries to form; wo_idx likewise for dWo
+    Returns a dict: QKV, O, out, dQKV, dX [len(rows), ...]; P {head: [len(rows), seq_len]};
+    dWqkv, dWo (the requested entries); dbqkv, dbo (whole); keep [len(rows), h].
+    """
+    T, h = X.shape
+    assert h % nh == 0 and nh % t == 0 and T % seq_len == 0
+    d = h // nh
+    n_seq = T // seq_len
+    rows = np.asarray(rows)
+    # forward projection, every token: slice i's columns of the Q, K and V blocks
+    QKV = np.empty((T, 3 * h))
+    for i in range(t):
+        cs = _slice_cols(h, t, i)
+        for blk in range(3):
+            for c0 in range(cs.start, cs.stop, col_block):
+                cols = slice(blk * h + c0, blk * h + min(c0 + col_block, cs.stop))
+                QKV[:, cols] = _rb(X @ Wqkv[:, cols] + bqkv[cols], mirror)
+    # output gradient of the block and the gradient reaching O (row split of Wo)
+    keep_all = dropout_keep(T, h, p, seed, token_offset)
+    dZ = _rb(np.where(keep_all, dOut * dropout_scale(p), 0.0), mirror)
+    dO = np.zeros((T, h))
+    for i in range(t):
+        rs = _slice_cols(h, t, i)
+        dO[:, rs] = dZ @ Wo[rs, :].T
+    dO = _rb(dO, mirror)
+    # per sequence and head: the forward attention and its backward
+    O = np.empty((T, h))
+    dQKV = np.empty((T, 3 * h))
+    P_rows = {j: np.zeros((len(rows), seq_len)) for j in heads}
+    causal = np.tril(np.ones((seq_len, seq_len), dtype=bool))
+    for s in range(n_seq):
+        rsl = slice(s * seq_len, (s + 1) * seq_len)
+        in_seq = np.nonzero((rows >= s * seq_len) & (rows < (s + 1) * seq_len))[0]
+        for j in range(nh):
+            qc = slice(j * d, (j + 1) * d)
+            kc = slice(h + j * d, h + (j + 1) * d)
+            vc = slice(2 * h + j * d, 2 * h + (j + 1) * d)
+            q, k, v = QKV[rsl, qc], QKV[rsl, kc], QKV[rsl, vc]
+            sc = np.where(causal, (q @ k.T) / math.sqrt(d), -np.inf)
+            e = np.exp(sc - sc.max(axis=1, keepdims=True))
+            pr = _rb(e / e.sum(axis=1, keepdims=True), mirror)
+            O[rsl, qc] = pr @ v
+            if j in P_rows:
+                P_rows[j][in_seq] = pr[rows[in_seq] - s * seq_len]
+            do = dO[rsl, qc]
+            dQKV[rsl, vc] = pr.T @ do
+            dp = do @ v.T
+            delta = (dp * pr).sum(axis=1, keepdims=True)
+            ds = _rb(pr * (dp - delta) / math.sqrt(d), mirror)
+            dQKV[rsl, qc] = ds @ k
+            dQKV[rsl, kc] = ds.T @ q
+    O = _rb(O, mirror)
+    dQKV = _rb(dQKV, mirror)
+    # block output rows: row split of Wo summed over slices, bias, dropout, residual
+    Zr = np.zeros((len(rows), h))
+    for i in range(t):
+        rs = _slice_cols(h, t, i)
+        Zr += O[rows][:, rs] @ Wo[rs, :]
+    keep = keep_all[rows]
+    out = _rb(X[rows] + np.where(keep, (Zr + bo) * dropout_scale(p), 0.0), mirror)
+    # input-gradient rows (operator f: sum over every column block of Wqkv)
+    dXs = np.zeros((len(rows), h))
+    for c0 in range(0, 3 * h, col_block):
+        cols = slice(c0, min(c0 + col_block, 3 * h))
+        dXs += dQKV[rows][:, cols] @ Wqkv[:, cols].T
+    dX = _rb(dOut[rows] + dXs, mirror)
+    r_q, c_q = (np.asarray(a) for a in wqkv_idx)
+    r_o, c_o = (np.asarray(a) for a in wo_idx)
+    dWqkv = np.array([X[:, r] @ dQKV[:, c] for r, c in zip(r_q, c_q)])
+    dWo = np.array([O[:, r] @ dZ[:, c] for r, c in zip(r_o, c_o)])
+    return {"QKV": QKV[rows], "O": O[rows], "out": out, "dQKV": dQKV[rows], "dX": dX, "P": P_rows,
+            "dWqkv": dWqkv, "dWo": dWo, "dbqkv": dQKV.sum(axis=0), "dbo": dZ.sum(axis=0), "keep": keep}

@@ -1,16 +1,23 @@
 """GPU parity of the tensor-sliced self-attention block (attn_fwd / attn_bwd)
 against the float64 oracle, through the C ABI.
 
-Bars: bf16 tensors (QKV, P, O, out, dQKV, dX) within max|gpu - oracle| /
-max|oracle| <= 1e-2 of both oracle modes, as for the MLP block.  fp32 accumulated
-gradients (dWqkv, dbqkv, dWo, dbo) within ATTN_F32_TOL = 5e-3 of the
-bf16-mirroring mode and 1e-2 of the pure mode: unlike the MLP's weight gradients
-(one bf16 storage point, dZ or dU, between the fp32 GEMMs), dWqkv is reached
-through four (dZ, dO, dS, dQKV), and the GPU's fp32 sums round to the other side
-of a bf16 step than the float64 mirror for a growing fraction of elements at each;
-those one-ulp (2^-8 relative) differences, summed over the tokens, measured up to
-2.0e-3 of the largest gradient.  Probabilities are exactly zero above the causal
-diagonal, and dropped outputs equal the residual exactly.
+Bars:
+  * bf16 tensors (QKV, P, O, out, dQKV, dX): max|gpu - oracle| / max|oracle| <= 1e-2
+    of both oracle modes, as for the MLP block;
+  * fp32 accumulated gradients (dWqkv, dbqkv, dWo, dbo): within 1e-2 of the pure
+    mode, and within max(1e-3, g) of the bf16-mirroring mode, where g is the
+    oracle's own distance between its pure and mirroring modes for that tensor on
+    the same inputs.  The mirroring mode rounds to bf16 at the block's storage
+    points from exact values; the block rounds at the same points from fp32
+    values, so it can land on the other side of a bf16 step wherever the exact
+    value is within fp32 error of a rounding boundary.  g measures the whole
+    effect of those storage roundings on the gradient (every element rounded,
+    through every point: QKV, P, O, dZ, dO, dS, dQKV for dWqkv), so a result no
+    farther from the mirror than the mirror is from the exact value is what the
+    storage precisions allow.  g comes from the oracle alone; it is 2.8e-3 to
+    3.7e-3 for dWqkv on the shapes below.
+  * Probabilities are exactly zero above the causal diagonal, and dropped outputs
+    equal the residual exactly.
 """
 import numpy as np
 import pytest
@@ -19,13 +26,12 @@ import torch
 from oracle import attn_oracle as ato
 from oracle import mlp_oracle as orc
 from transformer_lm_megatron_gb300 import build as gb_build
+from transformer_lm_megatron_gb300 import inputs as gin
 from transformer_lm_megatron_gb300 import mlp
 
-from gpu_harness import BF16_TOL, bits_f64, rel_err, to_f64
+from gpu_harness import BF16_TOL, F32_TOL, bits_f64, rel_err, to_f64
 
 pytestmark = pytest.mark.gpu
-
-ATTN_F32_TOL = 5e-3
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,6 +44,12 @@ def _weights(h, gen, std=0.02):
     def rnd(*shape, s=std):
         return (torch.randn(*shape, generator=gen) * s).to(torch.bfloat16)
     return rnd(h, 3 * h), rnd(3 * h), rnd(h, h), rnd(h)
+
+
+def f32_bar(pure, mirror) -> float:
+    """The fp32-gradient bar against the mirroring mode: the oracle's own
+    pure-to-mirror distance for the tensor, never below 1e-3."""
+    return max(F32_TOL, rel_err(mirror, pure))
 
 
 @pytest.fixture
@@ -73,8 +85,9 @@ def test_attention_block_full_parity(T, h, nh, t, L, k, cta_pair_mode):
     grads = {n: to_f64(getattr(buf, n)) for n in ("dWqkv", "dbqkv", "dWo", "dbo")}
 
     W64 = [bits_f64(x) for x in w]
+    acc = {}
     for mirror in (True, False):
-        acc = {n: 0.0 for n in grads}
+        acc[mirror] = {n: 0.0 for n in grads}
         for j, (X, dOut) in enumerate(mbs):
             X64, d64 = bits_f64(X), bits_f64(dOut)
             fw = ato.attn_fwd(X64, W64[0], W64[1], W64[2], W64[3], nh, t, L, p, seed, token_offset=j * T,
@@ -91,11 +104,80 @@ def test_attention_block_full_parity(T, h, nh, t, L, k, cta_pair_mode):
                 assert np.all(np.triu(P, k=1) == 0)
                 keep = fw["keep"]
                 np.testing.assert_array_equal(to_f64(g["out"])[~keep], X64[~keep])
-            for n in acc:
-                acc[n] = acc[n] + bw[n]
-        for n in grads:
-            e = rel_err(grads[n], acc[n])
-            assert e <= (ATTN_F32_TOL if mirror else BF16_TOL), (mirror, n, e)
+            for n in grads:
+                acc[mirror][n] = acc[mirror][n] + bw[n]
+    for n in grads:
+        assert rel_err(grads[n], acc[False][n]) <= BF16_TOL, ("pure", n)
+        bar = f32_bar(acc[False][n], acc[True][n])
+        e = rel_err(grads[n], acc[True][n])
+        assert e <= bar, ("mirror", n, e, bar)
+
+
+def _bits(t):
+    return gin.bf16_bits(t.detach().cpu())
+
+
+def test_attention_block_mtnlg_shape_sampled_parity():
+    """The benchmarked shape: h 20480, 128 heads (d = 160), t 8, one sequence of
+    2048 tokens, weights N(0, 0.02), the same seeded inputs the benchmark uses.
+    Checked at sampled positions, each computed by the oracle from its definition
+    (attn_sampled): token rows of QKV, O, out, dQKV, dX; the probability rows of
+    three heads at those tokens; 256 entries each of dWqkv and dWo; all of dbqkv
+    and dbo."""
+    c = gin.ATTN_MTNLG
+    h, nh, t, L, T = c["h"], c["nh"], c["t"], c["seq_len"], c["tokens"]
+    p, seed = 0.1, gin.DROPOUT_SEED
+    dev = torch.device("cuda")
+    w, X, dOut = gin.make_attn_inputs(h, T, device=dev)
+    buf = mlp.AttnBuffers(T, h, nh, L, device=dev)
+    mlp.attn_step(h, nh, t, L, p, seed, w, X, dOut, buf, accumulate=False)
+    torch.cuda.synchronize()
+    assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+
+    rng = np.random.default_rng(11)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 1023, T - 1], rng.integers(0, T, 4)]))
+    heads = [0, 61, nh - 1]
+    n_e = 256
+    rq = np.concatenate([[0, h - 1], rng.integers(0, h, n_e - 2)])
+    cq = np.concatenate([[0, 3 * h - 1], rng.integers(0, 3 * h, n_e - 2)])
+    ro = np.concatenate([[0, h - 1], rng.integers(0, h, n_e - 2)])
+    co = np.concatenate([[0, h - 1], rng.integers(0, h, n_e - 2)])
+    ridx = torch.from_numpy(rows).to(dev)
+    got = {"QKV": to_f64(buf.QKV.index_select(0, ridx)), "O": to_f64(buf.O.index_select(0, ridx)),
+           "out": to_f64(buf.out.index_select(0, ridx)), "dQKV": to_f64(buf.dQKV.index_select(0, ridx)),
+           "dX": to_f64(buf.dX.index_select(0, ridx)),
+           "dWqkv": to_f64(buf.dWqkv[torch.from_numpy(rq).to(dev), torch.from_numpy(cq).to(dev)]),
+           "dWo": to_f64(buf.dWo[torch.from_numpy(ro).to(dev), torch.from_numpy(co).to(dev)]),
+           "dbqkv": to_f64(buf.dbqkv), "dbo": to_f64(buf.dbo)}
+    P_got = {j: to_f64(buf.P[0, j].index_select(0, ridx)) for j in heads}
+
+    Wqkv = orc.Bf16Matrix(_bits(w[0]))
+    Wo = orc.Bf16Matrix(_bits(w[2]))
+    bqkv, bo = orc.bf16_to_f64(_bits(w[1])), orc.bf16_to_f64(_bits(w[3]))
+    X64, d64 = orc.bf16_to_f64(_bits(X)), orc.bf16_to_f64(_bits(dOut))
+    del buf, w
+    ref = {mirror: ato.attn_sampled(X64, d64, Wqkv, bqkv, Wo, bo, nh, t, L, p, seed, rows, heads, (rq, cq), (ro, co),
+                                    mirror=mirror)
+           for mirror in (True, False)}
+    for mirror in (True, False):
+        r = ref[mirror]
+        for name in ("QKV", "O", "out", "dQKV", "dX"):
+            e = rel_err(got[name], r[name])
+            assert e <= BF16_TOL, (mirror, name, e)
+        for j in heads:
+            e = rel_err(P_got[j], r["P"][j])
+            assert e <= BF16_TOL, (mirror, "P", j, e)
+    # causal: nothing above the diagonal; dropped outputs are the residual exactly
+    for j in heads:
+        for q, row in enumerate(rows):
+            assert np.all(P_got[j][q, row + 1:] == 0), (j, row)
+    keep = ref[True]["keep"]
+    np.testing.assert_array_equal(got["out"][~keep], X64[rows][~keep])
+    for name in ("dWqkv", "dWo", "dbqkv", "dbo"):
+        assert rel_err(got[name], ref[False][name]) <= BF16_TOL, ("pure", name)
+        bar = f32_bar(ref[False][name], ref[True][name])
+        e = rel_err(got[name], ref[True][name])
+        assert e <= bar, ("mirror", name, e, bar)
 
 
 def test_attention_rejects_bad_shapes():

@@ -12,7 +12,8 @@ from oracle import mlp_oracle as orc
 from transformer_lm_megatron_gb300 import build as gb_build
 from transformer_lm_megatron_gb300 import mlp
 
-from gpu_harness import (BF16_TOL, F32_TOL, Shape, compare_full, make_case, rel_err, run_gpu, run_oracle, to_f64)
+from gpu_harness import (BF16_TOL, F32_TOL, Shape, bits_f64, compare_full, make_case, rel_err, run_gpu,
+                         run_oracle, to_f64)
 
 pytestmark = pytest.mark.gpu
 
@@ -93,8 +94,10 @@ def test_ragged_shapes_full_parity(tokens, h, ffn, t, cta_pair_mode):
     s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2, p=0.1)
     w_dev, mbs_dev, w64, mbs64 = make_case(s)
     g_outs, g_grads = run_gpu(s, w_dev, mbs_dev)
-    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
-    compare_full(s, g_outs, g_grads, r_outs, r_grads, label=f"pair mode {cta_pair_mode}")
+    for mirror in (True, False):
+        r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=mirror)
+        compare_full(s, g_outs, g_grads, r_outs, r_grads, check_grads=mirror,
+                     label=f"pair mode {cta_pair_mode}, mirror={mirror}")
 
 
 @pytest.mark.parametrize("t", [2, 4, 8])
@@ -104,8 +107,9 @@ def test_one_slice_calls_full_parity(t):
     s = Shape(tokens=200, h=256, ffn=2048, t=t, k=2)
     w_dev, mbs_dev, w64, mbs64 = make_case(s)
     g_outs, g_grads = run_gpu(s, w_dev, mbs_dev, slice_mode="each")
-    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
-    compare_full(s, g_outs, g_grads, r_outs, r_grads, label=f"each t={t}")
+    for mirror in (True, False):
+        r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=mirror)
+        compare_full(s, g_outs, g_grads, r_outs, r_grads, check_grads=mirror, label=f"each t={t}, mirror={mirror}")
 
 
 def test_slice_invariance():
@@ -262,8 +266,10 @@ def test_split_tail_full_parity(tokens, h, ffn, t, cta_pair_mode):
     s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2, p=0.1)
     w_dev, mbs_dev, w64, mbs64 = make_case(s)
     g_outs, g_grads = run_gpu(s, w_dev, mbs_dev, keep_all=True)
-    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True, keep_all=True)
-    compare_full(s, g_outs, g_grads, r_outs, r_grads, label=f"split tail, pair mode {cta_pair_mode}")
+    for mirror in (True, False):
+        r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=mirror, keep_all=True)
+        compare_full(s, g_outs, g_grads, r_outs, r_grads, check_grads=mirror,
+                     label=f"split tail, pair mode {cta_pair_mode}, mirror={mirror}")
     again_outs, again_grads = run_gpu(s, w_dev, mbs_dev, keep_all=True)
     for j in range(s.k):
         for k in g_outs[j]:
@@ -308,3 +314,57 @@ def test_split_tail_on_concurrent_streams():
                 assert torch.equal(getattr(bufs[c], k).cpu(), ref[c][0][-1][k]), (rep, c, k)
             for k in ("dA", "da", "dB", "db"):
                 assert torch.equal(getattr(bufs[c], k).cpu(), ref[c][1][k]), (rep, c, k)
+
+
+@pytest.mark.parametrize("tokens,h,ffn,t,mode", [
+    (200, 136, 656, 2, "all"),      # ragged M, N and K tails, all slices per call
+    (200, 136, 656, 2, "each"),     # the same, one slice per call
+    (256, 512, 2048, 4, "each"),    # accumulation-sweep-like: four slices, one per call
+    (512, 1280, 2048, 1, "all"),    # split tail of F2 (dropout + residual) and B5 (input gradient)
+])
+def test_explicit_residual_and_no_residual_gradient(tokens, h, ffn, t, mode):
+    """mlp_fwd with a residual R that is not X, and mlp_bwd with residual_grad = 0
+    (dX = sum_i dU_i A_i^T, no dO term), against oracle.mlp_fwd(..., R=R) and
+    oracle.mlp_bwd(..., residual_is_input=False) in both modes, over two
+    accumulated micro-batches."""
+    s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2, p=0.1)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    gen = torch.Generator().manual_seed(77)
+    Rs = [torch.randn(tokens, h, generator=gen).to(torch.bfloat16) for _ in range(s.k)]
+    buf = mlp.BlockBuffers(tokens, h, ffn, t)
+    A, a, B, b = w_dev
+    slices = [-1] if mode == "all" else list(range(t))
+    outs = []
+    for j, (X, dO) in enumerate(mbs_dev):
+        R = Rs[j].cuda()
+        for i in slices:
+            mlp.mlp_fwd(h, ffn, t, i, tokens, s.p, s.seed, j * tokens, X, A, a, B, b, R, buf.U, buf.Y, buf.Zacc,
+                        buf.O)
+        for i in slices:
+            mlp.mlp_bwd(h, ffn, t, i, tokens, s.p, s.seed, j * tokens, 0, j > 0, dO, X, A, B, buf.U, buf.Y, buf.dZ,
+                        buf.dU, buf.dXacc, buf.dX, buf.dA, buf.da, buf.dB, buf.db)
+        outs.append({k: getattr(buf, k).cpu() for k in ("U", "Y", "O", "dZ", "dU", "dX")})
+    torch.cuda.synchronize()
+    assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+    grads = {k: getattr(buf, k).cpu() for k in ("dA", "da", "dB", "db")}
+    Aw, aw, Bw, bw = w64
+    for mirror in (True, False):
+        acc = {k: 0.0 for k in grads}
+        for j, (X64, dO64) in enumerate(mbs64):
+            R64 = bits_f64(Rs[j])
+            fw = orc.mlp_fwd(X64, Aw, aw, Bw, bw, t, s.p, s.seed, token_offset=j * tokens, R=R64, mirror=mirror)
+            bwd = orc.mlp_bwd(dO64, X64, Aw, Bw, fw["U"], fw["Y"], fw["keep"], t, s.p, mirror=mirror,
+                              residual_is_input=False)
+            ref = {**fw, **bwd}
+            for k in ("U", "Y", "O", "dZ", "dU", "dX"):
+                e = rel_err(to_f64(outs[j][k]), ref[k])
+                assert e <= BF16_TOL, (mirror, j, k, e)
+            # dropped outputs are the residual R exactly
+            O = to_f64(outs[j]["O"])
+            np.testing.assert_array_equal(O[~fw["keep"]], R64[~fw["keep"]])
+            for k in acc:
+                acc[k] = acc[k] + bwd[k]
+        if mirror:
+            for k in grads:
+                e = rel_err(to_f64(grads[k]), acc[k])
+                assert e <= F32_TOL, (k, e)

@@ -143,3 +143,30 @@ def test_planted_mistakes_are_caught():
             dQ[rows, j * d:(j + 1) * d] = ds @ QKV[rows, h + j * d:h + (j + 1) * d]
     bad_dWq = X.T @ dQ
     assert np.max(np.abs(bad_dWq - ref["dWqkv"][:, :h])) > 1e-6
+
+
+@pytest.mark.parametrize("mirror", [False, True])
+def test_sampled_evaluator_matches_full_oracle(mirror):
+    """attn_sampled (column-blocked weights, sampled entries) equals attn_fwd +
+    attn_bwd at every sampled position, also with the weights given as raw bf16
+    bits (Bf16Matrix), on a shape with two sequences and two slices."""
+    rng = np.random.default_rng(5)
+    T, h, nh, t, L, p = 48, 32, 4, 2, 24, 0.2
+    X, Wqkv, bqkv, Wo, bo, dOut = _inputs(T, h, rng)
+    fw = ato.attn_fwd(X, Wqkv, bqkv, Wo, bo, nh, t, L, p, 9, token_offset=3, mirror=mirror)
+    bw = ato.attn_bwd(dOut, X, Wqkv, Wo, fw["QKV"], fw["P"], fw["O"], fw["keep"], nh, t, L, p, mirror=mirror)
+    rows = np.array([0, 5, 23, 24, 47])
+    heads = [0, 3]
+    rq, cq = np.array([0, 31, 7]), np.array([0, 95, 50])
+    ro, co = np.array([1, 31]), np.array([0, 31])
+    for wq, wo in ((Wqkv, Wo), (orc.Bf16Matrix(orc.f64_to_bf16_bits(Wqkv)), orc.Bf16Matrix(orc.f64_to_bf16_bits(Wo)))):
+        s = ato.attn_sampled(X, dOut, wq, bqkv, wo, bo, nh, t, L, p, 9, rows, heads, (rq, cq), (ro, co),
+                             token_offset=3, mirror=mirror, col_block=5)
+        ref = {"QKV": fw["QKV"][rows], "O": fw["O"][rows], "out": fw["out"][rows], "dQKV": bw["dQKV"][rows],
+               "dX": bw["dX"][rows], "dWqkv": bw["dWqkv"][rq, cq], "dWo": bw["dWo"][ro, co], "dbqkv": bw["dbqkv"],
+               "dbo": bw["dbo"]}
+        for key, r in ref.items():
+            np.testing.assert_allclose(s[key], r, rtol=1e-12, atol=1e-12, err_msg=key)
+        np.testing.assert_array_equal(s["keep"], fw["keep"][rows])
+        for j in heads:
+            np.testing.assert_allclose(s["P"][j], fw["P"][rows // L, j, rows % L], rtol=1e-12, atol=1e-14)

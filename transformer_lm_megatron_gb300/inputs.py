@@ -91,3 +91,24 @@ def make_microbatch(tokens: int, h: int, j: int, device="cpu"):
 def bf16_bits(x: torch.Tensor):
     """The raw bf16 bit patterns of a CPU bf16 tensor as a numpy uint16 array."""
     return x.contiguous().cpu().view(torch.int16).numpy().view("uint16")
+
+
+# The self-attention block at the MT-NLG layer shape: hidden 20480, 128 heads
+# (head size 160), 8 slices, one sequence of 2048 tokens.
+ATTN_MTNLG = dict(h=20480, nh=128, t=8, seq_len=2048, tokens=2048)
+ATTN_SEED = 7
+
+
+def make_attn_inputs(h: int, tokens: int, device="cpu", seed: int = ATTN_SEED, std: float = WEIGHT_STD):
+    """Wqkv [h, 3h], bqkv [3h], Wo [h, h], bo [h] ~ N(0, std), then X [tokens, h]
+    and dOut [tokens, h] ~ N(0, 1), all from one generator seeded ``seed`` in that
+    order, drawn in fp32 and rounded to bf16."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    Wqkv = _normal_bf16((h, 3 * h), std, g, device)
+    bqkv = _normal_bf16((3 * h,), std, g, device)
+    Wo = _normal_bf16((h, h), std, g, device)
+    bo = _normal_bf16((h,), std, g, device)
+    X = _normal_bf16((tokens, h), 1.0, g, device)
+    dOut = _normal_bf16((tokens, h), 1.0, g, device)
+    return (Wqkv, bqkv, Wo, bo), X, dOut

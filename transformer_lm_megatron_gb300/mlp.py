@@ -258,8 +258,9 @@ class Trace:
             out[kind] = (c + 1, tot + t, fl + (2 * m * n * k if kind in GEMM_KINDS else 0))
         return out
 
-    def roofline(self, peaks, steps):
-        """The dominant kernel (the tcgen05 GEMM, all six contractions) against the bf16 tensor peak."""
+    def roofline(self, peak, peak_kind):
+        """The dominant kernel (the tcgen05 GEMM, all six contractions) against the bf16
+        tensor peak ``peak`` (TFLOP/s), described by ``peak_kind``."""
         summ = self.summary()
         g_launch = sum(summ[k][0] for k in GEMM_KINDS if k in summ)
         g_ms = sum(summ[k][1] for k in GEMM_KINDS if k in summ)
@@ -268,12 +269,11 @@ class Trace:
         if g_launch == 0 or g_ms <= 0:
             return None
         achieved = (g_flops / g_launch) / (g_ms / g_launch / 1e3) / 1e12
-        peak = peaks["bf16_sustained"]
         kernels = {TRACE_NAMES.get(k, str(k)): {"launches": v[0], "ms": round(v[1], 4),
                                                  "share": round(v[1] / all_ms, 4)} for k, v in sorted(summ.items())}
         return {"bound": "tensor", "kernel": "k_gemm_bf16_tc (tcgen05, all six GEMMs)", "achieved": achieved,
                 "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_kind": f"bf16 dense sustained ({peaks['source']})", "traffic": None,
+                "peak_kind": peak_kind, "traffic": None,
                 "flops_per_launch": g_flops / g_launch, "avg_launch_ms": g_ms / g_launch,
                 "gemm_share_of_kernel_time": g_ms / all_ms if all_ms else None, "kernels": kernels}
 
