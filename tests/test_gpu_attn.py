@@ -1,21 +1,26 @@
 """GPU parity of the tensor-sliced self-attention block (attn_fwd / attn_bwd)
 against the float64 oracle, through the C ABI.
 
-Bars:
-  * bf16 tensors (QKV, P, O, out, dQKV, dX): max|gpu - oracle| / max|oracle| <= 1e-2
-    of both oracle modes, as for the MLP block;
-  * fp32 accumulated gradients (dWqkv, dbqkv, dWo, dbo): within 1e-2 of the pure
-    mode, and within max(1e-3, g) of the bf16-mirroring mode, where g is the
-    oracle's own distance between its pure and mirroring modes for that tensor on
-    the same inputs.  The mirroring mode rounds to bf16 at the block's storage
-    points from exact values; the block rounds at the same points from fp32
-    values, so it can land on the other side of a bf16 step wherever the exact
-    value is within fp32 error of a rounding boundary.  g measures the whole
-    effect of those storage roundings on the gradient (every element rounded,
-    through every point: QKV, P, O, dZ, dO, dS, dQKV for dWqkv), so a result no
-    farther from the mirror than the mirror is from the exact value is what the
-    storage precisions allow.  g comes from the oracle alone; it is 2.8e-3 to
-    3.7e-3 for dWqkv on the shapes below.
+Bars, with g the oracle's own distance between its pure and bf16-mirroring modes
+for the tensor on the same inputs (max|mirror - pure| / max|pure|; it comes from
+the oracle alone):
+  * against the bf16-mirroring mode: bf16 tensors (QKV, P, O, out, dQKV, dX)
+    within max|gpu - oracle| / max|oracle| <= 1e-2, as for the MLP block; fp32
+    accumulated gradients (dWqkv, dbqkv, dWo, dbo) within max(1e-3, g).  The
+    mirroring mode rounds to bf16 at the block's storage points from exact values;
+    the block rounds at the same points from fp32 values, so it can land on the
+    other side of a bf16 step wherever the exact value is within fp32 error of a
+    rounding boundary.  g measures the whole effect of those storage roundings on
+    the gradient (every element rounded, through every point: QKV, P, O, dZ, dO,
+    dS, dQKV for dWqkv), so a result no farther from the mirror than the mirror is
+    from the exact value is what the storage precisions allow (g is 2.8e-3 to
+    3.7e-3 for dWqkv on the small shapes below).
+  * against the pure mode: the mirror bar plus g, which is what the triangle
+    inequality leaves for a result within the mirror bar.  At the MT-NLG shape
+    with N(0, 0.02) weights the scores have a standard deviation of about 8, so
+    the bf16 storage of Q and K alone moves the probabilities by about 1 %, and g
+    for O is about 1.6e-2: no implementation that stores QKV in bf16 can be within
+    1e-2 of the exact-arithmetic block there.
   * Probabilities are exactly zero above the causal diagonal, and dropped outputs
     equal the residual exactly.
 """
@@ -52,6 +57,12 @@ def f32_bar(pure, mirror) -> float:
     return max(F32_TOL, rel_err(mirror, pure))
 
 
+def pure_bar(mirror_bar, pure, mirror) -> float:
+    """The bar against the pure mode for a tensor held to ``mirror_bar`` against
+    the mirroring mode: that bar plus the oracle's pure-to-mirror distance."""
+    return mirror_bar + rel_err(mirror, pure)
+
+
 @pytest.fixture
 def cta_pair_mode(request):
     mlp.mlp_set_cta_pair(request.param)
@@ -85,32 +96,36 @@ def test_attention_block_full_parity(T, h, nh, t, L, k, cta_pair_mode):
     grads = {n: to_f64(getattr(buf, n)) for n in ("dWqkv", "dbqkv", "dWo", "dbo")}
 
     W64 = [bits_f64(x) for x in w]
-    acc = {}
-    for mirror in (True, False):
-        acc[mirror] = {n: 0.0 for n in grads}
-        for j, (X, dOut) in enumerate(mbs):
-            X64, d64 = bits_f64(X), bits_f64(dOut)
+    acc = {m: {n: 0.0 for n in grads} for m in (True, False)}
+    for j, (X, dOut) in enumerate(mbs):
+        X64, d64 = bits_f64(X), bits_f64(dOut)
+        ref = {}
+        for mirror in (True, False):
             fw = ato.attn_fwd(X64, W64[0], W64[1], W64[2], W64[3], nh, t, L, p, seed, token_offset=j * T,
                               mirror=mirror)
             bw = ato.attn_bwd(d64, X64, W64[0], W64[2], fw["QKV"], fw["P"], fw["O"], fw["keep"], nh, t, L, p,
                               mirror=mirror)
-            g = outs[j]
-            ref = {"QKV": fw["QKV"], "P": fw["P"], "O": fw["O"], "out": fw["out"], "dQKV": bw["dQKV"], "dX": bw["dX"]}
-            for name, r in ref.items():
-                e = rel_err(to_f64(g[name]), r)
-                assert e <= BF16_TOL, (mirror, j, name, e)
-            if mirror:
-                P = to_f64(g["P"])
-                assert np.all(np.triu(P, k=1) == 0)
-                keep = fw["keep"]
-                np.testing.assert_array_equal(to_f64(g["out"])[~keep], X64[~keep])
+            ref[mirror] = {"QKV": fw["QKV"], "P": fw["P"], "O": fw["O"], "out": fw["out"], "dQKV": bw["dQKV"],
+                           "dX": bw["dX"], "keep": fw["keep"]}
             for n in grads:
                 acc[mirror][n] = acc[mirror][n] + bw[n]
+        g = outs[j]
+        for name in ("QKV", "P", "O", "out", "dQKV", "dX"):
+            got = to_f64(g[name])
+            e = rel_err(got, ref[True][name])
+            assert e <= BF16_TOL, ("mirror", j, name, e)
+            e = rel_err(got, ref[False][name])
+            assert e <= pure_bar(BF16_TOL, ref[False][name], ref[True][name]), ("pure", j, name, e)
+        P = to_f64(g["P"])
+        assert np.all(np.triu(P, k=1) == 0)
+        keep = ref[True]["keep"]
+        np.testing.assert_array_equal(to_f64(g["out"])[~keep], X64[~keep])
     for n in grads:
-        assert rel_err(grads[n], acc[False][n]) <= BF16_TOL, ("pure", n)
         bar = f32_bar(acc[False][n], acc[True][n])
         e = rel_err(grads[n], acc[True][n])
         assert e <= bar, ("mirror", n, e, bar)
+        e = rel_err(grads[n], acc[False][n])
+        assert e <= pure_bar(bar, acc[False][n], acc[True][n]), ("pure", n, e)
 
 
 def _bits(t):
@@ -159,14 +174,18 @@ def test_attention_block_mtnlg_shape_sampled_parity():
     ref = {mirror: ato.attn_sampled(X64, d64, Wqkv, bqkv, Wo, bo, nh, t, L, p, seed, rows, heads, (rq, cq), (ro, co),
                                     mirror=mirror)
            for mirror in (True, False)}
-    for mirror in (True, False):
-        r = ref[mirror]
-        for name in ("QKV", "O", "out", "dQKV", "dX"):
-            e = rel_err(got[name], r[name])
-            assert e <= BF16_TOL, (mirror, name, e)
-        for j in heads:
-            e = rel_err(P_got[j], r["P"][j])
-            assert e <= BF16_TOL, (mirror, "P", j, e)
+    gaps = {}
+    for name in ("QKV", "O", "out", "dQKV", "dX"):
+        e = rel_err(got[name], ref[True][name])
+        assert e <= BF16_TOL, ("mirror", name, e)
+        e = rel_err(got[name], ref[False][name])
+        gaps[name] = rel_err(ref[True][name], ref[False][name])
+        assert e <= pure_bar(BF16_TOL, ref[False][name], ref[True][name]), ("pure", name, e, gaps[name])
+    for j in heads:
+        e = rel_err(P_got[j], ref[True]["P"][j])
+        assert e <= BF16_TOL, ("mirror", "P", j, e)
+        e = rel_err(P_got[j], ref[False]["P"][j])
+        assert e <= pure_bar(BF16_TOL, ref[False]["P"][j], ref[True]["P"][j]), ("pure", "P", j, e)
     # causal: nothing above the diagonal; dropped outputs are the residual exactly
     for j in heads:
         for q, row in enumerate(rows):
@@ -174,10 +193,11 @@ def test_attention_block_mtnlg_shape_sampled_parity():
     keep = ref[True]["keep"]
     np.testing.assert_array_equal(got["out"][~keep], X64[rows][~keep])
     for name in ("dWqkv", "dWo", "dbqkv", "dbo"):
-        assert rel_err(got[name], ref[False][name]) <= BF16_TOL, ("pure", name)
         bar = f32_bar(ref[False][name], ref[True][name])
         e = rel_err(got[name], ref[True][name])
         assert e <= bar, ("mirror", name, e, bar)
+        e = rel_err(got[name], ref[False][name])
+        assert e <= pure_bar(bar, ref[False][name], ref[True][name]), ("pure", name, e)
 
 
 def test_attention_rejects_bad_shapes():

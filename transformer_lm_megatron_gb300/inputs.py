@@ -58,6 +58,9 @@ WORKLOADS = {
     "sweep4": Workload("sweep4", tokens=2048, h=8192, ffn=32768, t=4, k=4),
     "sweep16": Workload("sweep16", tokens=2048, h=8192, ffn=32768, t=4, k=16),
     "sweep32": Workload("sweep32", tokens=2048, h=8192, ffn=32768, t=4, k=32),
+    # one of the MT-NLG layer's eight slices as a block of its own (A_i 20480 x 10240,
+    # B_i 10240 x 20480): 2.8 GB on the device, the size used for counter captures
+    "mtnlg_slice": Workload("mtnlg_slice", tokens=2048, h=20480, ffn=10240, t=1, k=1),
 }
 
 

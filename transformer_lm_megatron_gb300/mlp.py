@@ -284,7 +284,9 @@ class Trace:
 class BlockBuffers:
     """Activations, workspaces and fp32 gradient accumulators for one workload."""
 
-    def __init__(self, tokens: int, h: int, ffn: int, t: int, device="cuda"):
+    def __init__(self, tokens: int, h: int, ffn: int, t: int, device="cuda", grads=None):
+        """grads: optional (dA, da, dB, db) fp32 accumulators to use instead of new
+        ones, e.g. the views of one contiguous buffer (data_parallel.flat_gradients)."""
         bf = dict(dtype=torch.bfloat16, device=device)
         f32 = dict(dtype=torch.float32, device=device)
         self.U = torch.empty(tokens, ffn, **bf)
@@ -295,10 +297,10 @@ class BlockBuffers:
         self.dX = torch.empty(tokens, h, **bf)
         self.Zacc = torch.empty(tokens, h, **f32) if t > 1 else None
         self.dXacc = torch.empty(tokens, h, **f32) if t > 1 else None
-        self.dA = torch.zeros(h, ffn, **f32)
-        self.da = torch.zeros(ffn, **f32)
-        self.dB = torch.zeros(ffn, h, **f32)
-        self.db = torch.zeros(h, **f32)
+        if grads is None:
+            grads = (torch.zeros(h, ffn, **f32), torch.zeros(ffn, **f32), torch.zeros(ffn, h, **f32),
+                     torch.zeros(h, **f32))
+        self.dA, self.da, self.dB, self.db = grads
 
 
 def block_step(wl, weights, X, dO, buf: BlockBuffers, token_offset=0, slice_mode="all", stream=None,
