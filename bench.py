@@ -411,6 +411,7 @@ def run_ours(args, wl, rank, world, dist):
     dev = torch.device("cuda", local_rank)
     gb_build.build()
     mlp.load()
+    mlp.mlp_set_tile_scheduler(args.tile_scheduler == "dynamic")
 
     weights = gin.make_weights(wl.h, wl.ffn, device=dev)
     mbs = [gin.make_microbatch(wl.tokens, wl.h, j, device=dev) for j in range(wl.k)]
@@ -680,10 +681,11 @@ def run_ours(args, wl, rank, world, dist):
         # the nominal dense (no 2:4 sparsity) bf16 rate of a GB300, 2.25 PFLOP/s: the
         # stricter of the two denominators
         "pct_of_nominal_peak": 100.0 * value / (world * NOMINAL_BF16_DENSE_TFLOPS),
-        "config": dict(workload_config(wl, args.slice_mode, world),
-                       grad_init=("grad_accum_reset + every micro-batch adds (inside the timed region)"
-                                  if args.reset_each_step else
-                                  "first micro-batch of each step writes dA/da/dB/db, later ones add; no reset pass")),
+        "config": workload_config(wl, args.slice_mode, world),
+        "run": {"tile_order": args.tile_scheduler,
+                "grad_init": ("grad_accum_reset + every micro-batch adds (inside the timed region)"
+                              if args.reset_each_step else
+                              "first micro-batch of each step writes dA/da/dB/db, later ones add; no reset pass")},
         "gpu_launches": n_launch,
         "roofline": roofline,
         "cpu_baseline": cpu,
@@ -715,6 +717,8 @@ def main():
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention-block measurement")
     ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--tile-scheduler", default="dynamic", choices=["dynamic", "static"],
+                    help="order in which the GEMMs hand out output tiles (results are bit-identical)")
     ap.add_argument("--no-accumulate-form", action="store_true",
                     help="skip timing the += form (reset outside the timed region, every micro-batch adds)")
     ap.add_argument("--reset-each-step", action="store_true",

@@ -36,8 +36,9 @@
  *     module memory, held by every GPU that loads the library until the process
  *     exits: the 2-word status word; the split-tail partial sums and arrival
  *     counters of the GEMMs (4 regions of 304 x 2 x 32 x 256 fp32, about 20 MB
- *     each, see mlp_set_split_tail); and the 16 MiB fp32 array of
- *     mlp_fwd_static_scratch.
+ *     each, see mlp_set_split_tail); the tile counters of the GEMMs' dynamic
+ *     scheduler (2 ints per region, see mlp_set_tile_scheduler); and the 16 MiB
+ *     fp32 array of mlp_fwd_static_scratch.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
  *     and runs asynchronously.  A nonzero return means nothing was enqueued,
  *     except MLP_ECUDA, which reports a failed launch (later launches of the same
@@ -259,6 +260,20 @@ int mlp_set_dependent_launch(int enable);
  * GEMMs on further streams run unsplit.  Returns MLP_OK or MLP_EINVAL.
  */
 int mlp_set_split_tail(int enable);
+
+/*
+ * mlp_set_tile_scheduler - the order in which the persistent GEMM kernels hand
+ * out their output tiles, for later calls in this process: 1 (the default)
+ * dynamic, each CTA pair taking the next tile from a counter in global memory
+ * when it is ready for one, so that the pairs sharing an operand stripe start it
+ * together and the stripe is read from DRAM once; 0 static round-robin.  Results
+ * are bit-identical either way (a tile's arithmetic does not depend on which CTA
+ * computes it).  The counters are static device memory, one pair per stream
+ * region (the regions of mlp_set_split_tail); GEMMs on a fifth stream, GEMMs of
+ * one wave, and launches that overlap the previous kernel on their stream use the
+ * static order.  Returns MLP_OK or MLP_EINVAL.
+ */
+int mlp_set_tile_scheduler(int mode);
 
 /* mlp_launch_count - number of kernels this library has launched in this process. */
 uint64_t mlp_launch_count(void);

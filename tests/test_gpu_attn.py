@@ -208,3 +208,29 @@ def test_attention_rejects_bad_shapes():
     # head size not a multiple of 8, and tokens not a multiple of seq_len
     assert lib.attn_fwd(96, 16, 1, 64, 32, 0.1, 1, 0, *ptrs, None, *([x.data_ptr()] * 5), None) == mlp.MLP_EINVAL
     assert lib.attn_fwd(128, 4, 1, 60, 32, 0.1, 1, 0, *ptrs, None, *([x.data_ptr()] * 5), None) == mlp.MLP_EINVAL
+
+
+def test_attention_tile_scheduler_changes_no_bit():
+    """The batched attention products skip the tiles above the causal diagonal, so
+    the work per tile varies; the dynamic tile order balances it.  Results are
+    bit-identical to the static order."""
+    T, h, nh, t, L = 2048, 2048, 16, 8, 1024
+    gen = torch.Generator().manual_seed(5)
+    w = tuple(x.cuda() for x in _weights(h, gen, std=0.5 / np.sqrt(h)))
+    X = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
+    dOut = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
+    res = []
+    try:
+        for dynamic in (False, True, True):
+            mlp.mlp_set_tile_scheduler(dynamic)
+            buf = mlp.AttnBuffers(T, h, nh, L)
+            mlp.attn_step(h, nh, t, L, 0.1, 1234, w, X, dOut, buf, accumulate=False)
+            torch.cuda.synchronize()
+            assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+            res.append({n: getattr(buf, n).clone() for n in ("QKV", "P", "O", "out", "dQKV", "dX", "dWqkv", "dbqkv",
+                                                              "dWo", "dbo")})
+    finally:
+        mlp.mlp_set_tile_scheduler(True)
+    for r in res[1:]:
+        for n in r:
+            assert torch.equal(r[n], res[0][n]), n

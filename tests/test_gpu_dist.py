@@ -95,28 +95,35 @@ def test_gpipe_schedule_on_one_gpu():
     for a, b in zip(piped, seq):
         for x, y in zip((a.dA, a.da, a.dB, a.db), (b.dA, b.da, b.dB, b.db)):
             assert torch.equal(x, y)
-    # the oracle's chain of blocks (bf16-mirroring mode: each block's input is the
-    # previous block's stored bf16 output, each block's dO the next block's dX)
+    # the oracle's chain of blocks (each block's input is the previous block's
+    # output, each block's dO the next block's dX), in both modes.  A stage's
+    # gradients pass through the bf16 storage points of every later block (their
+    # dX), so the fp32-gradient bar against the mirroring mode is the oracle's own
+    # pure-to-mirror distance for that gradient, never below 1e-3 (the bar of one
+    # block), as for the attention block.
     W = [tuple(bits_f64(x.cpu()) for x in w) for w in weights]
-    acc = [{k: 0.0 for k in ("dA", "da", "dB", "db")} for _ in range(S)]
-    for j in range(m):
-        x = bits_f64(mbs[j][0].cpu())
-        saved = []
-        for s in range(S):
-            A, a, B, b = W[s]
-            fw = orc.mlp_fwd(x, A, a, B, b, wl.t, wl.p, 1234 + s, token_offset=j * wl.tokens, mirror=True)
-            saved.append((x, fw))
-            x = fw["O"]
-        assert rel_err(to_f64(outs[j]), x) <= BF16_TOL, j
-        g = bits_f64(mbs[j][1].cpu())
-        for s in reversed(range(S)):
-            A, a, B, b = W[s]
-            xs, fw = saved[s]
-            bw = orc.mlp_bwd(g, xs, A, B, fw["U"], fw["Y"], fw["keep"], wl.t, wl.p, mirror=True)
-            for k in acc[s]:
-                acc[s][k] = acc[s][k] + bw[k]
-            g = bw["dX"]
+    acc = {mirror: [{k: 0.0 for k in ("dA", "da", "dB", "db")} for _ in range(S)] for mirror in (True, False)}
+    for mirror in (True, False):
+        for j in range(m):
+            x = bits_f64(mbs[j][0].cpu())
+            saved = []
+            for s in range(S):
+                A, a, B, b = W[s]
+                fw = orc.mlp_fwd(x, A, a, B, b, wl.t, wl.p, 1234 + s, token_offset=j * wl.tokens, mirror=mirror)
+                saved.append((x, fw))
+                x = fw["O"]
+            assert rel_err(to_f64(outs[j]), x) <= BF16_TOL, (mirror, j)
+            g = bits_f64(mbs[j][1].cpu())
+            for s in reversed(range(S)):
+                A, a, B, b = W[s]
+                xs, fw = saved[s]
+                bw = orc.mlp_bwd(g, xs, A, B, fw["U"], fw["Y"], fw["keep"], wl.t, wl.p, mirror=mirror)
+                for k in acc[mirror][s]:
+                    acc[mirror][s][k] = acc[mirror][s][k] + bw[k]
+                g = bw["dX"]
     for s in range(S):
         for k, got in zip(("dA", "da", "dB", "db"), (piped[s].dA, piped[s].da, piped[s].dB, piped[s].db)):
-            e = rel_err(to_f64(got), acc[s][k])
-            assert e <= F32_TOL, (s, k, e)
+            bar = max(F32_TOL, rel_err(acc[True][s][k], acc[False][s][k]))
+            e = rel_err(to_f64(got), acc[True][s][k])
+            assert e <= bar, (s, k, e, bar)
+            assert rel_err(to_f64(got), acc[False][s][k]) <= BF16_TOL, (s, k)

@@ -368,3 +368,39 @@ def test_explicit_residual_and_no_residual_gradient(tokens, h, ffn, t, mode):
             for k in grads:
                 e = rel_err(to_f64(grads[k]), acc[k])
                 assert e <= F32_TOL, (k, e)
+
+
+@pytest.fixture
+def tile_scheduler():
+    yield
+    mlp.mlp_set_tile_scheduler(True)
+
+
+@pytest.mark.parametrize("cta_pair_mode", [0, 1], indirect=True, ids=["single", "pair"])
+@pytest.mark.parametrize("tokens,h,ffn,t,mode", [
+    (1000, 384, 1536, 4, "all"),     # several waves per GEMM
+    (1000, 384, 1536, 4, "each"),    # one-slice calls: fp32 partial sums through Zacc / dXacc
+    (512, 1280, 2048, 1, "all"),     # split tail (two half-reductions per tail tile)
+    (2304, 768, 3072, 1, "all"),     # many waves, ragged tails
+])
+def test_tile_scheduler_changes_no_bit(tokens, h, ffn, t, mode, cta_pair_mode, tile_scheduler):
+    """The dynamic tile order (a counter in global memory hands out the tiles) and
+    the static round-robin order give bit-identical results: a tile's arithmetic
+    does not depend on which CTA computes it.  Three accumulated micro-batches, so
+    the counters must come back to zero after every launch."""
+    s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=3)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    mlp.mlp_set_tile_scheduler(False)
+    o_st, g_st = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
+    mlp.mlp_set_tile_scheduler(True)
+    o_dy, g_dy = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
+    o_dy2, g_dy2 = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
+    for j in range(s.k):
+        for k in o_st[j]:
+            assert torch.equal(o_dy[j][k], o_st[j][k]), (j, k)
+            assert torch.equal(o_dy2[j][k], o_st[j][k]), (j, k)
+    for k in g_st:
+        assert torch.equal(g_dy[k], g_st[k]), k
+        assert torch.equal(g_dy2[k], g_st[k]), k
+    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
+    compare_full(s, [o_dy[-1]], g_dy, [r_outs[-1]], r_grads, label="dynamic tile order")

@@ -44,6 +44,9 @@ __device__ int g_status_word[2];
 constexpr int kSplitRegions = 4;
 __device__ float g_split_ws[kSplitRegions][kSplitSlots * 2 * kSplitSlotFloats];
 __device__ int g_split_flags[kSplitRegions][kSplitSlots];
+// Tile counters of the GEMMs' dynamic scheduler, one pair per stream region (the
+// same regions as the split tail): both 0 between launches.
+__device__ int g_sched_ctr[kSplitRegions][2];
 
 thread_local std::string g_last_error;
 std::atomic<uint64_t> g_launches{0};
@@ -104,6 +107,7 @@ struct DeviceState {
   int* status = nullptr;
   float* split_ws = nullptr;   // partial sums of the GEMMs' split tail, kSplitRegions regions
   int* split_flags = nullptr;
+  int* sched_ctr = nullptr;    // tile counters of the dynamic scheduler, 2 per region
   cudaStream_t split_owner[kSplitRegions] = {};  // the stream each region belongs to
   int split_regions_used = 0;
   bool gemm_attr[32] = {};  // per GEMM instantiation: dynamic smem attribute set
@@ -139,11 +143,14 @@ int device_state(DeviceState** out) {
     if (e != cudaSuccess) return fail(MLP_ECUDA, "status word address: %s", cudaGetErrorString(e));
     void* ws = nullptr;
     void* flags = nullptr;
+    void* ctr = nullptr;
     e = cudaGetSymbolAddress(&ws, g_split_ws);
     if (e == cudaSuccess) e = cudaGetSymbolAddress(&flags, g_split_flags);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&ctr, g_sched_ctr);
     if (e != cudaSuccess) return fail(MLP_ECUDA, "split-tail workspace address: %s", cudaGetErrorString(e));
     st.split_ws = static_cast<float*>(ws);
     st.split_flags = static_cast<int*>(flags);
+    st.sched_ctr = static_cast<int*>(ctr);
     if (g_encode == nullptr) {
       void* fn = nullptr;
       cudaDriverEntryPointQueryResult q;
@@ -162,8 +169,10 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The split-tail region of `stream` (assigned on first use), or -1 once all
-// regions belong to other streams; GEMMs on such a stream run without the split.
+// The region of `stream` (assigned on first use) in the static per-stream
+// workspaces (split-tail partial sums, tile counters), or -1 once all regions
+// belong to other streams; GEMMs on such a stream run without the split tail and
+// with the static tile order.
 std::mutex g_split_mu;
 int split_region(DeviceState* st, cudaStream_t stream) {
   std::lock_guard<std::mutex> lock(g_split_mu);
@@ -696,8 +705,9 @@ int mlp_sync_status(void* stream) {
   if (word[0] != 0) {
     const int zero[2] = {0, 0};
     cudaMemcpy(st->status, zero, sizeof(zero), cudaMemcpyHostToDevice);
-    // a launch that gave up may have left split-tail counters behind
+    // a launch that gave up may have left split-tail or tile counters behind
     cudaMemset(st->split_flags, 0, sizeof(int) * kSplitSlots * kSplitRegions);
+    cudaMemset(st->sched_ctr, 0, sizeof(int) * 2 * kSplitRegions);
     return fail(word[0], "a kernel gave up on a bounded wait (site %d)", word[1]);
   }
   return MLP_OK;
@@ -750,6 +760,12 @@ int mlp_set_cta_pair(int mode) {
 int mlp_set_dependent_launch(int enable) {
   if (enable != 0 && enable != 1) return fail(MLP_EINVAL, "mlp_set_dependent_launch: %d not in {0, 1}", enable);
   g_pdl.store(enable, std::memory_order_relaxed);
+  return MLP_OK;
+}
+
+int mlp_set_tile_scheduler(int mode) {
+  if (mode != 0 && mode != 1) return fail(MLP_EINVAL, "mlp_set_tile_scheduler: %d not in {0, 1}", mode);
+  g_tile_sched.store(mode, std::memory_order_relaxed);
   return MLP_OK;
 }
 

@@ -19,6 +19,8 @@ std::atomic<int> g_pair_mode{-1};
 std::atomic<int> g_epi_pace{1};
 std::atomic<int> g_late_wait{1};
 std::atomic<int> g_split_tail{1};
+// 1: dynamic tile order (a counter per stream region), 0: static round-robin.
+std::atomic<int> g_tile_sched{1};
 
 // Late dependency waits pay only for short GEMMs: there the next launch's tiles
 // fill the partial last wave and the pipeline drain of the one before.  Tiles are
@@ -147,18 +149,24 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
       items = tiles + rem;
     }
   }
+  // Dynamic tile order: the stream's tile counters, unless this launch may overlap
+  // the previous kernel on the stream (late wait), or the GEMM is one wave.
+  const int units_launched = (int)(items < units ? items : units);
+  int* sched = nullptr;
+  if (g_tile_sched.load(std::memory_order_relaxed) && !late_wait && items > units_launched) {
+    const int region = split_region(st, stream);
+    if (region >= 0) sched = st->sched_ctr + 2 * region;
+  }
   const int ts = trace_pre(stream);
   cudaError_t e;
   if (PAIR) {
-    const int pairs = (int)(items < st->max_pairs[slot] ? items : st->max_pairs[slot]);
-    e = launch_kernel(kern, dim3(2 * (unsigned)pairs), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, 2, 1, mA, mB, mC,
-                      mO0, mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
-                      st->status);
+    e = launch_kernel(kern, dim3(2 * (unsigned)units_launched), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, 2, 1, mA,
+                      mB, mC, mO0, mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal,
+                      late_wait ? 1 : 0, sched, st->status);
   } else {
-    const int grid = (int)(items < st->sms ? items : st->sms);
-    e = launch_kernel(kern, dim3((unsigned)grid), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, 1, 1, mA, mB, mC, mO0,
-                      mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal, late_wait ? 1 : 0,
-                      st->status);
+    e = launch_kernel(kern, dim3((unsigned)units_launched), dim3(Cfg::kThreads), Cfg::kSmemBytes, stream, 1, 1, mA, mB,
+                      mC, mO0, mO1, M, N, K, epx, raster_n_fast, group, l2_hints, batch, nb_h, causal,
+                      late_wait ? 1 : 0, sched, st->status);
   }
   trace_post(ts, stream, trace_kind, M, N, K);
   g_launches.fetch_add(1, std::memory_order_relaxed);

@@ -12,10 +12,14 @@
 //               tcgen05.mma.cta_group::2 issued by the even CTA: each CTA loads
 //               its own 128 rows of A and its half (128) of B's columns, so per
 //               SM the B traffic (smem and L2) halves; 6-stage ring of 32 KB.
-// (Batched GEMMs: 3 and 5 stages, see GemmCfg.)  The grid is persistent: CTAs
-// (pairs) take work items round-robin; an item is a tile, or, in the split tail
-// of a GEMM whose last wave would be at most half full, one half of a tile's
-// reduction (see EpiParams).
+// (Batched GEMMs: 3 and 5 stages, see GemmCfg.)  The grid is persistent.  An
+// item of work is a tile, or, in the split tail of a GEMM whose last wave would
+// be at most half full, one half of a tile's reduction (see EpiParams).  CTAs
+// (pairs) take items either round-robin (static) or, with a tile counter in
+// global memory, each the next one when it is ready for it (dynamic: the CTAs
+// that share an operand stripe then start it together instead of drifting apart
+// over the waves of a long GEMM, so the stripe is read from DRAM once and served
+// from L2 to the others).
 //
 // Warp roles (192 threads, or 320 in the wide configuration; one CTA per SM):
 //   warp 0      TMA producer: loads A/B k-blocks into the smem ring.
@@ -48,6 +52,10 @@ constexpr int kBK = 64;
 constexpr uint32_t kABytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kChunkBytes = 64 * kBK * 2;  // one 64 x BK box of an MN-major operand
 constexpr uint32_t kTmemCols = 2 * kBN;         // double-buffered accumulator
+// Dynamic tile scheduling: the even CTA's producer draws items from a counter in
+// global memory and hands them to every other role of both CTAs through a ring of
+// kItemDepth slots in shared memory.
+constexpr int kItemDepth = 4;
 // Outputs leave through TMA: each epilogue warp stages 32 rows x 32 columns in
 // one of two buffers and issues a bulk store (or, for fp32, a bulk reduce-add).
 // fp32 boxes are 4 KB with a 128-byte swizzle.
@@ -282,6 +290,10 @@ __device__ __forceinline__ void record_status(int* status, int code, int site) {
 // while the larger operand streams past them.
 // l2_hints: L2 policy of the A loads (bits 0-1), the B loads (bits 2-3) and the
 // output stores (bits 4-5), an L2Hint each (kL2None: no hint).
+// sched: null for the static round-robin order, else two ints in global memory,
+// both 0 at launch: [0] the next item to hand out, [1] the CTAs (pairs) that have
+// finished drawing; the last to finish sets both back to 0 for the next launch
+// (which may not touch them before this grid completes: no late wait).
 // BATCHED: `batch` independent GEMMs of the same M, N, K; every tensor map is 4-D
 // (x, y, hb, sb) with batch b = sb * nb_h + hb; only TMA-only epilogues and the softmax gradient.
 // causal (batched attention products, M and N or K indexing positions in one
@@ -294,7 +306,8 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmO0,
                    const __grid_constant__ CUtensorMap tmO1, int M, int N, int K, EpiParams ep, int raster_n_fast,
-                   int group, int l2_hints, int batch, int nb_h, int causal, int late_wait, int* status) {
+                   int group, int l2_hints, int batch, int nb_h, int causal, int late_wait, int* sched,
+                   int* status) {
   using Cfg = GemmCfg<PAIR, BATCHED || WIDE>;
   constexpr int kStages = Cfg::kStages;
   constexpr int kEpiWarps = Cfg::kEpiWarps;
@@ -311,6 +324,9 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
   uint64_t* mma_done = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   uint64_t* in_full = mma_done + 2;  // per epilogue warp, kInDepth: staged input boxes
+  uint64_t* item_full = in_full + kEpiWarps * kInDepth;  // dynamic scheduling: item ring
+  uint64_t* item_empty = item_full + kItemDepth;
+  int* s_item = reinterpret_cast<int*>(item_empty + kItemDepth);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -341,6 +357,12 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
     }
     mbar_init(mma_done, 1);
     for (int i = 0; i < kEpiWarps * kInDepth; ++i) mbar_init(&in_full[i], 1);
+    for (int i = 0; i < kItemDepth; ++i) {
+      mbar_init(&item_full[i], 1);
+      // consumers: the MMA issuer and the epilogue warps of the even CTA; the
+      // producer and the epilogue warps of the odd CTA (they arrive remotely)
+      mbar_init(&item_empty[i], PAIR ? 2 + 2 * kEpiWarps : 1 + kEpiWarps);
+    }
     fence_mbar_init();
   }
   const bool tma_out = epi_f32_out(ep.kind);
@@ -451,6 +473,52 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
     return true;
   };
 
+  // ---- the sequence of items each role works through.  Item n of this CTA
+  // (pair): static, unit + n * num_units; dynamic, the n-th item the even CTA's
+  // producer drew from the counter, read from ring slot n % kItemDepth.  -1 ends
+  // the sequence.  Every wait is bounded; a role that gives up records the
+  // timeout and sees -1.
+  const bool dynamic = sched != nullptr;
+  // Even CTA's producer: draw item n from the counter and publish it to both CTAs.
+  auto draw_item = [&](uint32_t n) -> int {
+    const int slot = (int)(n % kItemDepth);
+    if (!mbar_wait_cluster(&item_empty[slot], ((n / kItemDepth) & 1) ^ 1)) {
+      record_status(status, kStatusTimeout, 8);
+      return -1;
+    }
+    int item = atomicAdd(&sched[0], 1);
+    if (item >= item_end) item = -1;
+    s_item[slot] = item;
+    if constexpr (PAIR) {
+      asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa_shared(smem_u32(&s_item[slot]), 1)), "r"(item)
+                   : "memory");
+      mbar_arrive_cluster(mapa_shared(smem_u32(&item_full[slot]), 1));
+    }
+    mbar_arrive(&item_full[slot]);
+    return item;
+  };
+  // Every other role: item n as published.  release: free the slot (one arrival
+  // per role: `whole_warp` roles call this from all 32 lanes and lane 0 arrives
+  // once they have all read it; single-thread roles arrive themselves); a peek
+  // (release = false) leaves the slot to the later read that releases it.
+  auto read_item = [&](uint32_t n, bool release, bool whole_warp) -> int {
+    const int slot = (int)(n % kItemDepth);
+    if (!mbar_wait_cluster(&item_full[slot], (n / kItemDepth) & 1)) {
+      record_status(status, kStatusTimeout, 9);
+      return -1;
+    }
+    const int item = *reinterpret_cast<volatile int*>(&s_item[slot]);
+    if (release) {
+      if (whole_warp) __syncwarp();
+      if (!whole_warp || (threadIdx.x & 31) == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&item_empty[slot]), 0));
+    }
+    return item;
+  };
+  auto static_item = [&](uint32_t n) -> int {
+    const int item = unit + (int)n * num_units;
+    return item < item_end ? item : -1;
+  };
+
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
@@ -464,7 +532,9 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int item = unit; item < item_end && ok; item += num_units) {
+      for (uint32_t n_item = 0; ok; ++n_item) {
+        const int item = !dynamic ? static_item(n_item) : rank == 0 ? draw_item(n_item) : read_item(n_item, true, false);
+        if (item < 0) break;
         int m0, n0, hb, sb, kb0, kb1, half;
         if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
         const int b_n0 = n0 + (PAIR ? (int)rank * Cfg::kBLoadN : 0);
@@ -567,6 +637,14 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(10000);
       }
+      if (dynamic && rank == 0) {
+        // this CTA (pair) draws no more; the last one to finish resets the counter
+        __threadfence();
+        if (atomicAdd(&sched[1], 1) == num_units - 1) {
+          atomicExch(&sched[0], 0);
+          atomicExch(&sched[1], 0);
+        }
+      }
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -577,7 +655,9 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int item = unit; item < item_end && ok; item += num_units) {
+      for (uint32_t n_item = 0; ok; ++n_item) {
+        const int item = dynamic ? read_item(n_item, true, false) : static_item(n_item);
+        if (item < 0) break;
         int m0, n0, hb, sb, kb0, kb1, half;
         if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
         if (!(PAIR ? mbar_wait_cluster(&acc_empty[acc], acc_phase ^ 1) : mbar_wait(&acc_empty[acc], acc_phase ^ 1))) {
@@ -671,16 +751,21 @@ __global__ void __launch_bounds__(GemmCfg<PAIR, BATCHED || WIDE>::kThreads, 1)
     auto wait_in = [&](uint32_t i) {
       if (!mbar_wait(&my_in_full[i % kInDepth], (i / kInDepth) & 1)) record_status(status, kStatusTimeout, 7);
     };
-    for (int item = unit; item < item_end; item += num_units) {
+    for (uint32_t n_item = 0;; ++n_item) {
+      const int item = dynamic ? read_item(n_item, true, true) : static_item(n_item);
+      if (item < 0) break;
       int m0, n0, hb, sb, kb0, kb1, half;
       if (!item_info(item, m0, n0, hb, sb, kb0, kb1, half)) continue;
       kb_end += (uint32_t)max(kb1 - kb0, 0);
       // Reduction length of this CTA's next item, whose main loop these stores
-      // are spread over (0: no next item, the stores go out at once).
+      // are spread over (0: no next item, the stores go out at once).  With the
+      // dynamic order the next item is drawn while this one's copies are issued,
+      // long before this epilogue, so the peek does not wait in practice.
       uint32_t nkb_next = 0;
-      if (item + num_units < item_end) {
+      const int next = dynamic ? read_item(n_item + 1, false, true) : static_item(n_item + 1);
+      if (next >= 0) {
         int m1, n1, hb1, sb1, a0, a1, half1;
-        if (item_info(item + num_units, m1, n1, hb1, sb1, a0, a1, half1)) nkb_next = (uint32_t)max(a1 - a0, 0);
+        if (item_info(next, m1, n1, hb1, sb1, a0, a1, half1)) nkb_next = (uint32_t)max(a1 - a0, 0);
       }
       // column blocks of this warp that produce output (the rest are clipped)
       const bool rows_in = m0 + quarter * 32 < M;

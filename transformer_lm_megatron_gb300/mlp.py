@@ -43,6 +43,7 @@ _SIGNATURES = {
     "mlp_set_cta_pair": (_i32, [_i32]),
     "mlp_set_dependent_launch": (_i32, [_i32]),
     "mlp_set_split_tail": (_i32, [_i32]),
+    "mlp_set_tile_scheduler": (_i32, [_i32]),
     "adam_step": (_i32, [_i64, _vp, _f32, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i32, _vp]),
     "attn_fwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64] + [_vp] * 11 + [_vp]),
     "attn_bwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64, _i32, _i32] + [_vp] * 17 + [_vp]),
@@ -220,6 +221,10 @@ def mlp_set_dependent_launch(enable: bool):
 
 def mlp_set_split_tail(enable: bool):
     _check(load().mlp_set_split_tail(1 if enable else 0))
+
+
+def mlp_set_tile_scheduler(dynamic: bool):
+    _check(load().mlp_set_tile_scheduler(1 if dynamic else 0))
 
 
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
