@@ -717,7 +717,7 @@ def main():
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention-block measurement")
     ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
-    ap.add_argument("--tile-scheduler", default="dynamic", choices=["dynamic", "static"],
+    ap.add_argument("--tile-scheduler", default="static", choices=["dynamic", "static"],
                     help="order in which the GEMMs hand out output tiles (results are bit-identical)")
     ap.add_argument("--no-accumulate-form", action="store_true",
                     help="skip timing the += form (reset outside the timed region, every micro-batch adds)")

@@ -373,7 +373,7 @@ def test_explicit_residual_and_no_residual_gradient(tokens, h, ffn, t, mode):
 @pytest.fixture
 def tile_scheduler():
     yield
-    mlp.mlp_set_tile_scheduler(True)
+    mlp.mlp_set_tile_scheduler(False)
 
 
 @pytest.mark.parametrize("cta_pair_mode", [0, 1], indirect=True, ids=["single", "pair"])

@@ -19,8 +19,10 @@ std::atomic<int> g_pair_mode{-1};
 std::atomic<int> g_epi_pace{1};
 std::atomic<int> g_late_wait{1};
 std::atomic<int> g_split_tail{1};
-// 1: dynamic tile order (a counter per stream region), 0: static round-robin.
-std::atomic<int> g_tile_sched{1};
+// 1: dynamic tile order (a counter per stream region), 0: static round-robin (the
+// default: measured on the MT-NLG layer, the dynamic order changed no DRAM traffic
+// and was 2 % slower, its weight-gradient GEMMs 9 %).
+std::atomic<int> g_tile_sched{0};
 
 // Late dependency waits pay only for short GEMMs: there the next launch's tiles
 // fill the partial last wave and the pipeline drain of the one before.  Tiles are
