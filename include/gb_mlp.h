@@ -263,10 +263,11 @@ int mlp_set_split_tail(int enable);
 
 /*
  * mlp_set_tile_scheduler - the order in which the persistent GEMM kernels hand
- * out their output tiles, for later calls in this process: 0 (the default)
- * static round-robin; 1 dynamic, each CTA pair taking the next tile from a
- * counter in global memory when it is ready for one, so that the pairs sharing an
- * operand stripe start it together.  Results
+ * out their output tiles, for later calls in this process: 0 static round-robin;
+ * 1 dynamic, each CTA pair taking the next tile from a counter in global memory
+ * when it is ready for one (this balances GEMMs whose tiles carry unequal work);
+ * -1 (the default) dynamic for the batched causal attention products, static for
+ * every other GEMM.  Results
  * are bit-identical either way (a tile's arithmetic does not depend on which CTA
  * computes it).  The counters are static device memory, one pair per stream
  * region (the regions of mlp_set_split_tail); GEMMs on a fifth stream, GEMMs of

@@ -226,8 +226,8 @@ def test_attention_tile_scheduler_changes_no_bit():
     dOut = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
     res = []
     try:
-        for dynamic in (False, True, True):
-            mlp.mlp_set_tile_scheduler(dynamic)
+        for mode in (0, 1, -1):
+            mlp.mlp_set_tile_scheduler(mode)
             buf = mlp.AttnBuffers(T, h, nh, L)
             mlp.attn_step(h, nh, t, L, 0.1, 1234, w, X, dOut, buf, accumulate=False)
             torch.cuda.synchronize()
@@ -235,7 +235,7 @@ def test_attention_tile_scheduler_changes_no_bit():
             res.append({n: getattr(buf, n).clone() for n in ("QKV", "P", "O", "out", "dQKV", "dX", "dWqkv", "dbqkv",
                                                               "dWo", "dbo")})
     finally:
-        mlp.mlp_set_tile_scheduler(False)
+        mlp.mlp_set_tile_scheduler(-1)
     for r in res[1:]:
         for n in r:
             assert torch.equal(r[n], res[0][n]), n

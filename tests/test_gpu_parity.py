@@ -373,7 +373,7 @@ def test_explicit_residual_and_no_residual_gradient(tokens, h, ffn, t, mode):
 @pytest.fixture
 def tile_scheduler():
     yield
-    mlp.mlp_set_tile_scheduler(False)
+    mlp.mlp_set_tile_scheduler(-1)
 
 
 @pytest.mark.parametrize("cta_pair_mode", [0, 1], indirect=True, ids=["single", "pair"])
@@ -390,9 +390,9 @@ def test_tile_scheduler_changes_no_bit(tokens, h, ffn, t, mode, cta_pair_mode, t
     the counters must come back to zero after every launch."""
     s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=3)
     w_dev, mbs_dev, w64, mbs64 = make_case(s)
-    mlp.mlp_set_tile_scheduler(False)
+    mlp.mlp_set_tile_scheduler(0)
     o_st, g_st = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
-    mlp.mlp_set_tile_scheduler(True)
+    mlp.mlp_set_tile_scheduler(1)
     o_dy, g_dy = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
     o_dy2, g_dy2 = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
     for j in range(s.k):

@@ -764,7 +764,7 @@ int mlp_set_dependent_launch(int enable) {
 }
 
 int mlp_set_tile_scheduler(int mode) {
-  if (mode != 0 && mode != 1) return fail(MLP_EINVAL, "mlp_set_tile_scheduler: %d not in {0, 1}", mode);
+  if (mode < -1 || mode > 1) return fail(MLP_EINVAL, "mlp_set_tile_scheduler: %d not in {-1, 0, 1}", mode);
   g_tile_sched.store(mode, std::memory_order_relaxed);
   return MLP_OK;
 }

@@ -19,10 +19,12 @@ std::atomic<int> g_pair_mode{-1};
 std::atomic<int> g_epi_pace{1};
 std::atomic<int> g_late_wait{1};
 std::atomic<int> g_split_tail{1};
-// 1: dynamic tile order (a counter per stream region), 0: static round-robin (the
-// default: measured on the MT-NLG layer, the dynamic order changed no DRAM traffic
-// and was 2 % slower, its weight-gradient GEMMs 9 %).
-std::atomic<int> g_tile_sched{0};
+// Tile order: 1 dynamic (a counter per stream region) for every GEMM, 0 static
+// round-robin for every GEMM, -1 (the default) dynamic for the batched attention
+// products only.  Measured: on the MT-NLG MLP block the dynamic order changed no
+// DRAM traffic and was 2 % slower (its weight-gradient GEMMs 9 %); on the causal
+// attention products, whose tiles carry unequal work, it was 4-9 % faster.
+std::atomic<int> g_tile_sched{-1};
 
 // Late dependency waits pay only for short GEMMs: there the next launch's tiles
 // fill the partial last wave and the pipeline drain of the one before.  Tiles are
@@ -155,7 +157,8 @@ int launch_gemm_t(DeviceState* st, const CUtensorMap& mA, const CUtensorMap& mB,
   // the previous kernel on the stream (late wait), or the GEMM is one wave.
   const int units_launched = (int)(items < units ? items : units);
   int* sched = nullptr;
-  if (g_tile_sched.load(std::memory_order_relaxed) && !late_wait && items > units_launched) {
+  const int order = g_tile_sched.load(std::memory_order_relaxed);
+  if ((order == 1 || (order < 0 && BATCHED)) && !late_wait && items > units_launched) {
     const int region = split_region(st, stream);
     if (region >= 0) sched = st->sched_ctr + 2 * region;
   }

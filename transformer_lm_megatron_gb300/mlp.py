@@ -223,8 +223,10 @@ def mlp_set_split_tail(enable: bool):
     _check(load().mlp_set_split_tail(1 if enable else 0))
 
 
-def mlp_set_tile_scheduler(dynamic: bool):
-    _check(load().mlp_set_tile_scheduler(1 if dynamic else 0))
+def mlp_set_tile_scheduler(mode: int):
+    """1 dynamic tile order for every GEMM, 0 static for every GEMM, -1 (default)
+    dynamic for the batched attention products only."""
+    _check(load().mlp_set_tile_scheduler(int(mode)))
 
 
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
