@@ -170,7 +170,9 @@ int adam_step(int64_t n, const float* grad, float grad_scale, float* master, flo
  *   X, R, O, out [tokens, h]; Wqkv [h, 3h] = [Wq | Wk | Wv] with head j at columns
  *   j*d .. (j+1)*d of each block; bqkv [3h]; Wo [h, h]; bo [h]  (bf16).
  *   QKV [tokens, 3h] bf16 (saved), P [n_seq, nh, seq_len, seq_len] bf16 (saved
- *   probabilities), O [tokens, h] bf16 (saved), S: fp32 workspace of P's shape.
+ *   probabilities, exact zeros above the diagonal), O [tokens, h] bf16 (saved),
+ *   S: fp32 workspace of P's shape (not touched by the fused core, see
+ *   mlp_set_attn_fused, but always required).
  * Returns MLP_OK or an error code.
  */
 int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_t seed, uint64_t token_offset,
@@ -262,6 +264,18 @@ int mlp_set_dependent_launch(int enable);
 int mlp_set_split_tail(int enable);
 
 /*
+ * mlp_set_attn_fused - choose, for later attn_fwd calls in this process, how the
+ * attention core runs: 1 (the default) one fused kernel per call when the head
+ * size d is at most 192 (S = Q K^T / sqrt(d) stays in tensor memory; two passes
+ * over the key tiles, the first for each row's maximum and sum, the second writing
+ * the normalised bf16 P and accumulating O = P V; the S workspace is not touched);
+ * 0 three launches with S in HBM (a batched GEMM, the row softmax, a batched GEMM).
+ * P and O agree within a bf16 rounding step of P (the softmax sums run in another
+ * order).  Returns MLP_OK or MLP_EINVAL.
+ */
+int mlp_set_attn_fused(int enable);
+
+/*
  * mlp_set_tile_scheduler - the order in which the persistent GEMM kernels hand
  * out their output tiles, for later calls in this process: 0 static round-robin;
  * 1 dynamic, each CTA pair taking the next tile from a counter in global memory
@@ -292,7 +306,8 @@ int mlp_trace_begin(int capacity);
  * max_entries of them in launch order: kinds[i] (0..5 = the GEMMs F1, F2, B2, B3,
  * B4, B5 of the forward/backward; 10 = dropout backward + db; 11 = column sum
  * for da; 12 = accumulator reset; 14 = adam_step; 20 = attention GEMMs; 21 =
- * softmax forward / backward), mnk[3i..3i+2] = the launch's M, N, K (GEMMs)
+ * softmax forward / backward; 22 = fused attention core), mnk[3i..3i+2] = the
+ * launch's M, N, K (GEMMs; for the fused core: query rows, keys per sequence, d)
  * or rows, columns, 0, and ms[i] = its device time in milliseconds.  Any output
  * pointer may be NULL.  Returns the number of entries written, or an error code.
  */

@@ -70,6 +70,14 @@ def cta_pair_mode(request):
     mlp.mlp_set_cta_pair(-1)
 
 
+@pytest.fixture
+def attn_core(request):
+    mlp.mlp_set_attn_fused(request.param == "fused")
+    yield request.param
+    mlp.mlp_set_attn_fused(True)
+
+
+@pytest.mark.parametrize("attn_core", ["fused", "unfused"], indirect=True)
 @pytest.mark.parametrize("cta_pair_mode", [0, 1], indirect=True, ids=["single", "pair"])
 @pytest.mark.parametrize("T,h,nh,t,L,k", [
     (256, 256, 4, 2, 128, 2),     # two sequences, d = 64, two accumulated micro-batches
@@ -78,7 +86,7 @@ def cta_pair_mode(request):
     (2048, 256, 2, 2, 2048, 1),    # one sequence of 2048: the longest rows the warp-per-row softmax holds
     (2304, 128, 2, 1, 2304, 1),    # rows past 2048 columns: the CTA-per-row softmax
 ])
-def test_attention_block_full_parity(T, h, nh, t, L, k, cta_pair_mode):
+def test_attention_block_full_parity(T, h, nh, t, L, k, cta_pair_mode, attn_core):
     p, seed = 0.1, 1234
     gen = torch.Generator().manual_seed(21)
     w = _weights(h, gen, std=0.5 / np.sqrt(h))
@@ -239,3 +247,39 @@ def test_attention_tile_scheduler_changes_no_bit():
     for r in res[1:]:
         for n in r:
             assert torch.equal(r[n], res[0][n]), n
+
+
+@pytest.mark.parametrize("T,h,nh,L", [
+    (2048, 2048, 16, 1024),   # d = 128, two sequences
+    (1088, 640, 4, 136),      # d = 160 (three 64-column atoms, the last half used), ragged 136-token sequences
+    (384, 640, 8, 384),       # d = 80: a head size that is not a multiple of 64
+])
+def test_fused_core_agrees_with_unfused(T, h, nh, L):
+    """The fused core (S on chip, two passes) and the three-launch core compute the
+    same P and O: P within one bf16 step (its softmax sums run in another order),
+    O, the block output and dQKV within the bf16 bar; P is exactly zero above the
+    diagonal.  (Both cores are compared with the oracle in the parity tests.)"""
+    gen = torch.Generator().manual_seed(9)
+    w = tuple(x.cuda() for x in _weights(h, gen, std=0.5 / np.sqrt(h)))
+    X = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
+    dOut = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
+    res = {}
+    try:
+        for fused in (False, True):
+            mlp.mlp_set_attn_fused(fused)
+            buf = mlp.AttnBuffers(T, h, nh, L)
+            buf.P.fill_(float("nan"))       # the fused core must write every entry, zeros included
+            mlp.attn_step(h, nh, 1, L, 0.1, 1234, w, X, dOut, buf, accumulate=False)
+            torch.cuda.synchronize()
+            assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+            res[fused] = {n: to_f64(getattr(buf, n)) for n in ("P", "O", "out", "dQKV")}
+    finally:
+        mlp.mlp_set_attn_fused(True)
+    Pf, Pu = res[True]["P"], res[False]["P"]
+    assert np.all(np.isfinite(Pf))
+    assert np.all(np.abs(Pf - Pu) <= 2.0 ** -8 * np.abs(Pu) + 1e-30)
+    for i in range(Pf.shape[0]):
+        for j in range(Pf.shape[1]):
+            assert np.all(np.triu(Pf[i, j], k=1) == 0)
+    for n in ("O", "out", "dQKV"):
+        assert rel_err(res[True][n], res[False][n]) <= BF16_TOL, n

@@ -1,0 +1,442 @@
+// Fused causal attention core of the self-attention block's forward, for one GB300
+// (sm_103a): per (sequence, head) and tile of 128 queries,
+//
+//   S = Q K^T / sqrt(d)   (keys <= query),   P = softmax(S),   O_head = P V
+//
+// with S kept on chip.  The block's heads are the column split of the fused QKV
+// projection (tensor slicing, "STRONGHOLD" slides items 7-8, read for attention
+// as in the block's header); each head attends causally within its sequence (a
+// left-to-right decoder with 128 heads: jiqizhixin article on MT-NLG).
+//
+// Two passes over the key tiles 0 .. i of query tile i:
+//   pass 1  S_j = Q K_j^T into tensor memory; each query row keeps its running
+//           maximum m and sum l = sum_k exp(s_k - m) (rescaled when m grows);
+//   pass 2  S_j again; P_j = exp(S_j - m) / l, rounded to bf16, goes to shared
+//           memory, where it is the A operand of O += P_j V_j, and to global memory
+//           (the backward reads P); the O accumulator in tensor memory then holds
+//           the final O, with no rescaling.
+// P is written as exact zeros above the causal diagonal, as the unfused path does.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over the work items, the
+// items with the most key tiles first):
+//   warp 0     TMA producer: Q (once per item), then K_0 .. K_i (pass 1), then
+//              K_0, K_1, V_0, K_2, V_1, ... (pass 2) through a 2-slot ring.
+//   warp 1     TMEM owner and MMA issuer (one thread): S into two 128-column
+//              buffers; in pass 2 S_{j+1} is issued before O += P_j V_j so the
+//              softmax of one tile overlaps the products of the next.
+//   warps 2-5  one query row per thread (TMEM lane quarter warp % 4): the softmax,
+//              the bf16 P tile, the zeros above the diagonal, and the bf16 O.
+// Every wait is bounded; on timeout the kernel records kStatusTimeout in the
+// status word and stops.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "gemm_tc.cuh"
+#include "ptx.cuh"
+
+namespace gbmlp {
+
+constexpr int kFaTile = 128;                         // queries per tile; keys per key tile
+constexpr int kFaMaxAtoms = 3;                       // head size d <= 192 (64 columns per atom)
+constexpr uint32_t kFaAtomBytes = 128 * 128;         // 128 rows x 64 bf16
+constexpr uint32_t kFaTileBytes = kFaMaxAtoms * kFaAtomBytes;   // a Q, K or V tile: 48 KB
+constexpr int kFaStages = 2;                         // K / V ring
+constexpr uint32_t kFaPBytes = 2 * kFaAtomBytes;     // P tile, 128 x 128 bf16
+constexpr uint32_t kFaOStageBytes = 32 * 32 * 2;     // one 32 x 32 bf16 output box
+constexpr int kFaThreads = 192;
+constexpr uint32_t kFaTmemCols = 512;                // S buffers at 0 and 128, O at 256
+constexpr size_t kFaSmemBytes = (size_t)kFaTileBytes * (1 + kFaStages) + 2 * kFaPBytes +
+                                4 * 2 * kFaOStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+static_assert(kFaSmemBytes <= 232448, "smem budget");
+
+struct FaParams {
+  int L;          // sequence length (keys and queries per sequence)
+  int nh;         // heads
+  int ns;         // sequences
+  int d;          // head size
+  int d_pad;      // d rounded up to 16 (the N of O += P V)
+  int n_atoms;    // ceil(d_pad / 64)
+  float alpha;    // 1 / sqrt(d)
+  uint16_t* P;    // [ns, nh, L, L] bf16
+};
+
+// maps: mQ, mK (box 64 x 128), mV (box 64 x 64) over QKV viewed as
+// (d, L, nh, ns); mP (box 64 x 32) over P as (L, L, nh, ns); mO (box 32 x 32,
+// 64-byte swizzle) over O as (d, L, nh, ns).
+__global__ void __launch_bounds__(kFaThreads, 1)
+    k_attn_fwd_fused(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                     const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mP,
+                     const __grid_constant__ CUtensorMap mO, FaParams fp, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = sQ + kFaTileBytes;
+  uint8_t* sP = sRing + kFaStages * kFaTileBytes;
+  uint8_t* sO = sP + 2 * kFaPBytes;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sO + 4 * 2 * kFaOStageBytes);
+  uint64_t* q_full = bar;
+  uint64_t* q_empty = bar + 1;
+  uint64_t* kv_full = bar + 2;                 // [kFaStages]
+  uint64_t* kv_empty = kv_full + kFaStages;    // [kFaStages]
+  uint64_t* s_full = kv_empty + kFaStages;     // [2]
+  uint64_t* s_empty = s_full + 2;              // [2]
+  uint64_t* p_full = s_empty + 2;              // [2]
+  uint64_t* p_empty = p_full + 2;              // [2]
+  uint64_t* o_full = p_empty + 2;
+  uint64_t* o_empty = o_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_qt = (fp.L + kFaTile - 1) / kFaTile;
+  const int heads = fp.nh * fp.ns;
+  const int num_items = n_qt * heads;
+  const uint32_t tile_tx = (uint32_t)fp.n_atoms * kFaAtomBytes;   // bytes of one Q, K or V tile
+
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kFaStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&s_empty[b], 4);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&p_empty[b], 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(o_empty, 4);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mK);
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mP);
+    tma_prefetch_desc(&mO);
+  }
+  if (warp == 1) {
+    tmem_alloc<false>(tmem_slot, kFaTmemCols);
+    tmem_relinquish<false>();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (threadIdx.x == 0) s_skip = (status != nullptr && *reinterpret_cast<volatile int*>(status) != 0) ? 1 : 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int item_end = s_skip ? 0 : num_items;
+
+  // item -> (query tile, head, sequence): the tiles with the most key tiles first
+  auto decode = [&](int item, int& qt, int& hb, int& sb) {
+    qt = n_qt - 1 - item / heads;
+    const int r = item % heads;
+    hb = r % fp.nh;
+    sb = r / fp.nh;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t kv = 0;  // ring uses so far
+      bool ok = true;
+      uint32_t n_item = 0;
+      for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x, ++n_item) {
+        int qt, hb, sb;
+        decode(item, qt, hb, sb);
+        const int nkv = qt + 1;
+        const int q0 = qt * kFaTile;
+        if (!mbar_wait(q_empty, (n_item & 1) ^ 1)) {
+          record_status(status, kStatusTimeout, 20);
+          break;
+        }
+        mbar_arrive_expect_tx(q_full, tile_tx);
+        for (int a = 0; a < fp.n_atoms; ++a) tma_load_4d(sQ + a * kFaAtomBytes, &mQ, q_full, 64 * a, q0, hb, sb);
+        // pass 1: K_0 .. K_{nkv-1}; pass 2: K_0, then K_{j+1} (if any) and V_j for each j
+        auto load_k = [&](int j) -> bool {
+          const int s = (int)(kv % kFaStages);
+          if (!mbar_wait(&kv_empty[s], ((kv / kFaStages) & 1) ^ 1)) return false;
+          uint8_t* dst = sRing + s * kFaTileBytes;
+          mbar_arrive_expect_tx(&kv_full[s], tile_tx);
+          for (int a = 0; a < fp.n_atoms; ++a)
+            tma_load_4d(dst + a * kFaAtomBytes, &mK, &kv_full[s], 64 * a, j * kFaTile, hb, sb);
+          ++kv;
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          const int s = (int)(kv % kFaStages);
+          if (!mbar_wait(&kv_empty[s], ((kv / kFaStages) & 1) ^ 1)) return false;
+          uint8_t* dst = sRing + s * kFaTileBytes;
+          mbar_arrive_expect_tx(&kv_full[s], tile_tx);
+          // MN-major B operand of O += P V: two halves of 64 keys, each n_atoms chunks of 64 head columns
+          for (int hk = 0; hk < 2; ++hk)
+            for (int c = 0; c < fp.n_atoms; ++c)
+              tma_load_4d(dst + (hk * fp.n_atoms + c) * 8192, &mV, &kv_full[s], 64 * c, j * kFaTile + 64 * hk, hb,
+                          sb);
+          ++kv;
+          return true;
+        };
+        for (int j = 0; j < nkv && ok; ++j) ok = load_k(j);
+        if (ok) ok = load_k(0);
+        for (int j = 0; j < nkv && ok; ++j) {
+          if (j + 1 < nkv) ok = load_k(j + 1);
+          if (ok) ok = load_v(j);
+        }
+        if (!ok) record_status(status, kStatusTimeout, 21);
+      }
+      // Drain: every copy this CTA issued has landed before the CTA may exit (the
+      // last use of each barrier completes the phase of parity (uses - 1) & 1).
+      if (n_item > 0 && !mbar_wait(q_full, (n_item - 1) & 1)) record_status(status, kStatusTimeout, 24);
+      for (uint32_t s = 0; s < (uint32_t)kFaStages; ++s) {
+        const uint32_t uses = kv / kFaStages + (s < kv % kFaStages ? 1u : 0u);
+        if (uses > 0 && !mbar_wait(&kv_full[s], (uses - 1) & 1)) record_status(status, kStatusTimeout, 25);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_s = make_idesc_bf16(kFaTile, kFaTile, false, false);
+      const uint32_t idesc_o = make_idesc_bf16(kFaTile, fp.d_pad, false, true);
+      const int nk_s = fp.d_pad / 16;  // k-steps of S = Q K^T
+      uint32_t kv = 0, sc = 0, pc = 0;
+      bool ok = true;
+      uint32_t n_item = 0;
+      auto wait_kv = [&]() -> uint8_t* {
+        const int s = (int)(kv % kFaStages);
+        if (!mbar_wait(&kv_full[s], (kv / kFaStages) & 1)) return nullptr;
+        tc_fence_after();
+        return sRing + s * kFaTileBytes;
+      };
+      auto release_kv = [&]() {
+        umma_commit(&kv_empty[kv % kFaStages]);
+        ++kv;
+      };
+      // S_j = Q K_j^T into S buffer sc % 2
+      auto issue_s = [&]() -> bool {
+        uint8_t* kt = wait_kv();
+        if (kt == nullptr) return false;
+        const int b = (int)(sc & 1);
+        if (!mbar_wait(&s_empty[b], ((sc >> 1) & 1) ^ 1)) return false;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(b * kFaTile);
+        const uint32_t qb = smem_u32(sQ), kb = smem_u32(kt);
+        for (int kk = 0; kk < nk_s; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kFaAtomBytes + (uint32_t)(kk & 3) * 32;
+          umma_bf16(d_tmem, make_sdesc_sw128(qb + off, 16, 1024), make_sdesc_sw128(kb + off, 16, 1024), idesc_s,
+                    kk > 0 ? 1u : 0u);
+        }
+        release_kv();
+        umma_commit(&s_full[b]);
+        ++sc;
+        return true;
+      };
+      // O (+)= P_j V_j
+      auto issue_o = [&](bool first) -> bool {
+        uint8_t* vt = wait_kv();
+        if (vt == nullptr) return false;
+        const int b = (int)(pc & 1);
+        if (!mbar_wait(&p_full[b], (pc >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t o_tmem = tmem_base + 256u;
+        const uint32_t pb = smem_u32(sP + b * kFaPBytes), vb = smem_u32(vt);
+        for (int kk = 0; kk < kFaTile / 16; ++kk) {
+          const uint32_t aoff = (uint32_t)(kk >> 2) * kFaAtomBytes + (uint32_t)(kk & 3) * 32;
+          const uint32_t boff = (uint32_t)(kk >> 2) * (uint32_t)fp.n_atoms * 8192u + (uint32_t)(kk & 3) * 2048u;
+          umma_bf16(o_tmem, make_sdesc_sw128(pb + aoff, 16, 1024), make_sdesc_sw128(vb + boff, 8192, 1024), idesc_o,
+                    (first && kk == 0) ? 0u : 1u);
+        }
+        release_kv();
+        umma_commit(&p_empty[b]);
+        ++pc;
+        return true;
+      };
+      for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x, ++n_item) {
+        int qt, hb, sb;
+        decode(item, qt, hb, sb);
+        const int nkv = qt + 1;
+        if (!mbar_wait(q_full, n_item & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int j = 0; j < nkv && ok; ++j) ok = issue_s();          // pass 1
+        if (ok) ok = issue_s();                                       // pass 2: S_0
+        if (ok && nkv == 1) umma_commit(q_empty);
+        if (ok && !mbar_wait(o_empty, (n_item & 1) ^ 1)) ok = false;  // the previous item's O has been read
+        tc_fence_after();
+        for (int j = 0; j < nkv && ok; ++j) {
+          if (j + 1 < nkv) {
+            ok = issue_s();                                           // S_{j+1} ahead of O += P_j V_j
+            if (ok && j + 2 == nkv) umma_commit(q_empty);             // Q read for the last time
+          }
+          if (ok) ok = issue_o(j == 0);
+        }
+        if (ok) umma_commit(o_full);
+      }
+      if (!ok) record_status(status, kStatusTimeout, 22);
+    }
+  } else {
+    // -------------------------------------------------------------- softmax / epilogue
+    const int quarter = warp & 3;
+    const int r_in = quarter * 32 + lane;                  // query row within the tile
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* my_o = sO + (warp - 2) * 2 * kFaOStageBytes;
+    uint32_t sc = 0, pc = 0, n_out = 0;
+    bool ok = true;
+    uint32_t n_item = 0;
+    auto wait_s = [&]() -> bool {
+      const int b = (int)(sc & 1);
+      if (!mbar_wait(&s_full[b], (sc >> 1) & 1)) return false;
+      tc_fence_after();
+      return true;
+    };
+    auto release_s = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[sc & 1]);
+      ++sc;
+    };
+    for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x, ++n_item) {
+      int qt, hb, sb;
+      decode(item, qt, hb, sb);
+      const int nkv = qt + 1;
+      const int q = qt * kFaTile + r_in;                   // query index in the sequence
+      const bool row_ok = q < fp.L;
+      // zeros above the diagonal: this warp's rows, keys (qt + 1) * 128 .. L - 1
+      {
+        const int c_begin = nkv * kFaTile;
+        const int z = fp.L - c_begin;
+        if (z > 0) {
+          for (int rr = 0; rr < 32; ++rr) {
+            const int qq = qt * kFaTile + quarter * 32 + rr;
+            if (qq >= fp.L) break;
+            uint16_t* row = fp.P + (((int64_t)sb * fp.nh + hb) * fp.L + qq) * (int64_t)fp.L + c_begin;
+            for (int c = lane * 8; c < z; c += 256) *reinterpret_cast<uint4*>(row + c) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      // pass 1: running maximum and sum of the row
+      float m = -INFINITY, l = 0.0f;
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!(ok = wait_s())) break;
+        const uint32_t t_s = t_lane + (uint32_t)((sc & 1) * kFaTile);
+        const bool diag = j == qt;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_s + c0, r);
+          tmem_ld_wait();
+          float v[32];
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            v[k] = (diag && c0 + k > r_in) ? -INFINITY : fp.alpha * __uint_as_float(r[k]);
+            mx = fmaxf(mx, v[k]);
+          }
+          const float m_new = fmaxf(m, mx);
+          float s = 0.0f;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) s += __expf(v[k] - m_new);
+          l = (m == -INFINITY ? 0.0f : l * __expf(m - m_new)) + s;
+          m = m_new;
+        }
+        release_s();
+      }
+      const float inv = 1.0f / l;
+      // pass 2: P_j = exp(S_j - m) / l to shared memory (operand of O += P V) and to P
+      for (int j = 0; j < nkv && ok; ++j) {
+        if (!(ok = wait_s())) break;
+        const uint32_t t_s = t_lane + (uint32_t)((sc & 1) * kFaTile);
+        const int b = (int)(pc & 1);
+        // the buffer is free once the products that read it are done and this
+        // warp's store of it has read it
+        if (!(ok = mbar_wait(&p_empty[b], ((pc >> 1) & 1) ^ 1))) break;
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t* pbuf = sP + b * kFaPBytes;
+        const bool diag = j == qt;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_s + c0, r);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int k0 = 2 * k, k1 = 2 * k + 1;
+            const float p0 = (diag && c0 + k0 > r_in) ? 0.0f : __expf(fp.alpha * __uint_as_float(r[k0]) - m) * inv;
+            const float p1 = (diag && c0 + k1 > r_in) ? 0.0f : __expf(fp.alpha * __uint_as_float(r[k1]) - m) * inv;
+            pk[k] = pack_bf16x2(p0, p1);
+          }
+          // row r_in, keys c0 .. c0 + 31: chunks of 8 keys in the 128-byte swizzle of atom c0 / 64
+          uint8_t* atom = pbuf + (c0 >> 6) * kFaAtomBytes + r_in * 128;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int chunk = ((c0 & 63) >> 3) + g;
+            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r_in & 7)) << 4)) =
+                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+          }
+        }
+        release_s();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int a = 0; a < 2; ++a)
+            tma_store_4d(&mP, pbuf + a * kFaAtomBytes + quarter * 32 * 128, j * kFaTile + 64 * a,
+                         qt * kFaTile + quarter * 32, hb, sb);
+          bulk_commit();
+          mbar_arrive(&p_full[b]);
+        }
+        ++pc;
+      }
+      if (!ok) break;
+      // O: the accumulator is final; bf16 through 32 x 32 boxes
+      if (!(ok = mbar_wait(o_full, n_item & 1))) break;
+      tc_fence_after();
+      for (int c0 = 0; c0 < fp.d_pad; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_lane + 256u + (uint32_t)c0, r);
+        tmem_ld_wait();
+        if (c0 >= fp.d) continue;
+        uint8_t* box = my_o + (n_out & 1) * kFaOStageBytes;
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint32_t off = lane * 64 + ((g ^ ((lane >> 1) & 3)) << 4);
+          *reinterpret_cast<uint4*>(box + off) =
+              make_uint4(pack_bf16x2(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1])),
+                         pack_bf16x2(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3])),
+                         pack_bf16x2(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5])),
+                         pack_bf16x2(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7])));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_4d(&mO, box, c0, qt * kFaTile + quarter * 32, hb, sb);
+          bulk_commit();
+        }
+        ++n_out;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_empty);
+      (void)row_ok;
+    }
+    if (!ok) record_status(status, kStatusTimeout, 23);
+    if (lane == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<false>(tmem_base, kFaTmemCols);
+  }
+}
+
+}  // namespace gbmlp

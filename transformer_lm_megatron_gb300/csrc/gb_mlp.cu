@@ -27,6 +27,7 @@
 
 #include "adam.cuh"
 #include "attention.cuh"
+#include "attn_fused.cuh"
 #include "elementwise.cuh"
 #include "gb_mlp.h"
 #include "gemm_tc.cuh"
@@ -70,7 +71,7 @@ TraceState g_trace;
 enum TraceKind {
   kTraceF1 = 0, kTraceF2 = 1, kTraceB2 = 2, kTraceB3 = 3, kTraceB4 = 4, kTraceB5 = 5,
   kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13, kTraceAdam = 14,
-  kTraceAttnGemm = 20, kTraceSoftmax = 21
+  kTraceAttnGemm = 20, kTraceSoftmax = 21, kTraceAttnCore = 22
 };
 
 // Records the start event of the next launch; returns its slot or -1.
@@ -111,6 +112,7 @@ struct DeviceState {
   cudaStream_t split_owner[kSplitRegions] = {};  // the stream each region belongs to
   int split_regions_used = 0;
   bool gemm_attr[32] = {};  // per GEMM instantiation: dynamic smem attribute set
+  bool fa_attr = false;     // fused attention core: dynamic smem attribute set
   int max_pairs[32] = {};   // per CTA-pair instantiation: co-resident clusters of two
 };
 
@@ -490,6 +492,58 @@ int check_attn_shape(int h, int nh, int t, int64_t tokens, int seq_len, float p)
   return MLP_OK;
 }
 
+// 1 (the default): the attention forward's core (S = Q K^T, softmax, O = P V) runs
+// as one fused kernel when the head size is at most 192; 0: three launches with S
+// in HBM (a batched GEMM, the row softmax, a batched GEMM).
+std::atomic<int> g_attn_fused{1};
+
+// The fused attention core over every (sequence, head, query tile); P and O as in
+// attn_fwd.  Returns MLP_OK or an error code.
+int attn_core_fused(DeviceState* st, const uint16_t* QKV, uint16_t* P, uint16_t* O, int h, int nh, int L, int ns,
+                    cudaStream_t s) {
+  const int d = h / nh;
+  const int64_t h3 = 3 * (int64_t)h;
+  FaParams fp;
+  fp.L = L;
+  fp.nh = nh;
+  fp.ns = ns;
+  fp.d = d;
+  fp.d_pad = (d + 15) & ~15;
+  fp.n_atoms = (fp.d_pad + 63) / 64;
+  fp.alpha = 1.0f / std::sqrt((float)d);
+  fp.P = P;
+  CUtensorMap mQ, mK, mV, mP, mO;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  int rc = make_map4(&mQ, bf, 2, QKV, d, L, h3, nh, d, ns, L * h3, 64, kFaTile, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (!rc)
+    rc = make_map4(&mK, bf, 2, QKV + h, d, L, h3, nh, d, ns, L * h3, 64, kFaTile, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (!rc)
+    rc = make_map4(&mV, bf, 2, QKV + 2 * h, d, L, h3, nh, d, ns, L * h3, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (!rc)
+    rc = make_map4(&mP, bf, 2, P, L, L, L, nh, (int64_t)L * L, ns, (int64_t)nh * L * L, 64, 32,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (!rc)
+    rc = make_map4(&mO, bf, 2, O, d, L, h, nh, d, ns, (int64_t)L * h, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (rc) return rc;
+  if (!st->fa_attr) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_attn_fwd_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFaSmemBytes);
+    if (e != cudaSuccess) return fail(MLP_ECUDA, "cudaFuncSetAttribute (fused attention): %s", cudaGetErrorString(e));
+    st->fa_attr = true;
+  }
+  const int64_t items = (int64_t)((L + kFaTile - 1) / kFaTile) * nh * ns;
+  const unsigned grid = (unsigned)(items < st->sms ? items : st->sms);
+  const int ts = trace_pre(s);
+  const cudaError_t e = launch_kernel(k_attn_fwd_fused, dim3(grid), dim3(kFaThreads), kFaSmemBytes, s, 1, 1, mQ, mK,
+                                      mV, mP, mO, fp, st->status);
+  trace_post(ts, s, kTraceAttnCore, (int64_t)ns * nh * L, L, d);
+  return launch_check(e, "fused attention core");
+}
+
 int softmax_launch(DeviceState* st, const float* S, uint16_t* P, int64_t rows, int cols, cudaStream_t s) {
   int64_t blocks = rows < (int64_t)st->sms * 16 ? rows : (int64_t)st->sms * 16;
   const int ts = trace_pre(s);
@@ -566,6 +620,19 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   e.bias = bqkv;
   rc = gemm(st, X, false, h, Wqkv, true, h3, T, (int)h3, h, e, s, kTraceAttnGemm);
   if (rc) return rc;
+  if (g_attn_fused.load(std::memory_order_relaxed) && ((d + 15) & ~15) <= kFaMaxAtoms * 64) {
+    // S = Q K^T / sqrt(d), P = softmax(S), O = P V in one kernel; S stays on chip
+    rc = attn_core_fused(st, QKV, P, O, h, nh, L, ns, s);
+    if (rc) return rc;
+    EpiParams ezf{};
+    ezf.kind = kEpiDropRes;
+    ezf.ld = h;
+    ezf.in0 = R;
+    ezf.bias = bo;
+    ezf.out0 = out;
+    ezf.drop = make_dropout(p, seed, token_offset, h);
+    return gemm(st, O, false, h, Wo, true, h, T, h, h, ezf, s, kTraceAttnGemm);
+  }
   // S = Q K^T / sqrt(d), -inf above the diagonal; per (sequence, head)
   EpiParams es{};
   es.kind = kEpiScaleMask;
@@ -760,6 +827,12 @@ int mlp_set_cta_pair(int mode) {
 int mlp_set_dependent_launch(int enable) {
   if (enable != 0 && enable != 1) return fail(MLP_EINVAL, "mlp_set_dependent_launch: %d not in {0, 1}", enable);
   g_pdl.store(enable, std::memory_order_relaxed);
+  return MLP_OK;
+}
+
+int mlp_set_attn_fused(int enable) {
+  if (enable != 0 && enable != 1) return fail(MLP_EINVAL, "mlp_set_attn_fused: %d not in {0, 1}", enable);
+  g_attn_fused.store(enable, std::memory_order_relaxed);
   return MLP_OK;
 }
 

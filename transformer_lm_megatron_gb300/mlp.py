@@ -44,6 +44,7 @@ _SIGNATURES = {
     "mlp_set_dependent_launch": (_i32, [_i32]),
     "mlp_set_split_tail": (_i32, [_i32]),
     "mlp_set_tile_scheduler": (_i32, [_i32]),
+    "mlp_set_attn_fused": (_i32, [_i32]),
     "adam_step": (_i32, [_i64, _vp, _f32, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i32, _vp]),
     "attn_fwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64] + [_vp] * 11 + [_vp]),
     "attn_bwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64, _i32, _i32] + [_vp] * 17 + [_vp]),
@@ -223,6 +224,10 @@ def mlp_set_split_tail(enable: bool):
     _check(load().mlp_set_split_tail(1 if enable else 0))
 
 
+def mlp_set_attn_fused(enable: bool):
+    _check(load().mlp_set_attn_fused(1 if enable else 0))
+
+
 def mlp_set_tile_scheduler(mode: int):
     """1 dynamic tile order for every GEMM, 0 static for every GEMM, -1 (default)
     dynamic for the batched attention products only."""
@@ -232,7 +237,7 @@ def mlp_set_tile_scheduler(mode: int):
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
                3: "B3 gemm Y_i^T.dZ (+= dB)", 4: "B4 gemm X^T.dU_i (+= dA)", 5: "B5 gemm dU_i.A_i^T (+dO)",
                10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset", 14: "adam step",
-               20: "attention GEMM", 21: "softmax, softmax-grad row sums"}
+               20: "attention GEMM", 21: "softmax, softmax-grad row sums", 22: "fused attention core"}
 GEMM_KINDS = (0, 1, 2, 3, 4, 5)
 
 
