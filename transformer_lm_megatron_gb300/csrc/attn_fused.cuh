@@ -17,15 +17,17 @@
 //           the final O, with no rescaling.
 // P is written as exact zeros above the causal diagonal, as the unfused path does.
 //
-// Warp roles (192 threads, one CTA per SM, persistent over the work items, the
+// Warp roles (320 threads, one CTA per SM, persistent over the work items, the
 // items with the most key tiles first):
 //   warp 0     TMA producer: Q (once per item), then K_0 .. K_i (pass 1), then
 //              K_0, K_1, V_0, K_2, V_1, ... (pass 2) through a 2-slot ring.
 //   warp 1     TMEM owner and MMA issuer (one thread): S into two 128-column
 //              buffers; in pass 2 S_{j+1} is issued before O += P_j V_j so the
 //              softmax of one tile overlaps the products of the next.
-//   warps 2-5  one query row per thread (TMEM lane quarter warp % 4): the softmax,
-//              the bf16 P tile, the zeros above the diagonal, and the bf16 O.
+//   warps 2-9  one query row per thread (TMEM lane quarter warp % 4), two warps
+//              per row: each takes every other key tile for the softmax and the
+//              bf16 P tile, then half of the zeros above the diagonal and half of
+//              the bf16 O columns.
 // Every wait is bounded; on timeout the kernel records kStatusTimeout in the
 // status word and stops.
 #pragma once
@@ -44,11 +46,28 @@ constexpr uint32_t kFaTileBytes = kFaMaxAtoms * kFaAtomBytes;   // a Q, K or V t
 constexpr int kFaStages = 2;                         // K / V ring
 constexpr uint32_t kFaPBytes = 2 * kFaAtomBytes;     // P tile, 128 x 128 bf16
 constexpr uint32_t kFaOStageBytes = 32 * 32 * 2;     // one 32 x 32 bf16 output box
-constexpr int kFaThreads = 192;
+constexpr int kFaSoftmaxWarps = 8;                   // two per TMEM lane quarter
+constexpr int kFaThreads = 64 + 32 * kFaSoftmaxWarps;
 constexpr uint32_t kFaTmemCols = 512;                // S buffers at 0 and 128, O at 256
-constexpr size_t kFaSmemBytes = (size_t)kFaTileBytes * (1 + kFaStages) + 2 * kFaPBytes +
-                                4 * 2 * kFaOStageBytes + 1024 /*align*/ + 512 /*barriers*/;
+// Q, the K/V ring, two P buffers (which also stage the O stores at the end of an
+// item), barriers, and the softmax halves' partial maxima and sums.
+constexpr size_t kFaSmemBytes = (size_t)kFaTileBytes * (1 + kFaStages) + 2 * kFaPBytes + 1024 /*align*/ +
+                                256 /*barriers*/ + 2 * 128 * 2 * sizeof(float);
 static_assert(kFaSmemBytes <= 232448, "smem budget");
+static_assert(kFaSoftmaxWarps * 2 * kFaOStageBytes <= 2 * kFaPBytes, "O staging fits in the P buffers");
+constexpr float kLog2e = 1.4426950408889634f;      // log2(e): exp(x) = 2^(x log2 e)
+
+// 2^x with the hardware approximation (ex2.approx, flush-to-zero); 2^-inf = 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Barrier of the softmax warps only (named barrier 1; warps 2 .. 2 + kFaSoftmaxWarps - 1).
+__device__ __forceinline__ void fa_softmax_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * kFaSoftmaxWarps) : "memory");
+}
 
 struct FaParams {
   int L;          // sequence length (keys and queries per sequence)
@@ -73,8 +92,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint8_t* sQ = smem;
   uint8_t* sRing = sQ + kFaTileBytes;
   uint8_t* sP = sRing + kFaStages * kFaTileBytes;
-  uint8_t* sO = sP + 2 * kFaPBytes;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sO + 4 * 2 * kFaOStageBytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sP + 2 * kFaPBytes);
   uint64_t* q_full = bar;
   uint64_t* q_empty = bar + 1;
   uint64_t* kv_full = bar + 2;                 // [kFaStages]
@@ -104,12 +122,12 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], 4);
-      mbar_init(&p_full[b], 4);
+      mbar_init(&s_empty[b], kFaSoftmaxWarps / 2);   // the 4 warps of the half that read it
+      mbar_init(&p_full[b], kFaSoftmaxWarps / 2);
       mbar_init(&p_empty[b], 1);
     }
     mbar_init(o_full, 1);
-    mbar_init(o_empty, 4);
+    mbar_init(o_empty, kFaSoftmaxWarps);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -282,37 +300,29 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax / epilogue
+    // Two warps per TMEM lane quarter: the warp of half h takes the key tiles j
+    // with j % 2 == h.  Pass 1 gives each half a partial maximum and sum per row,
+    // merged through shared memory; pass 2 writes the P tiles of its key tiles;
+    // the O columns are shared out by 32-column block.
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int r_in = quarter * 32 + lane;                  // query row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    uint8_t* my_o = sO + (warp - 2) * 2 * kFaOStageBytes;
+    float* s_ml = reinterpret_cast<float*>(tmem_slot + 4);  // [2 halves][128 rows][m, l]
+    const float al = fp.alpha * kLog2e;                     // scores in units of log2
     uint32_t sc = 0, pc = 0, n_out = 0;
     bool ok = true;
     uint32_t n_item = 0;
-    auto wait_s = [&]() -> bool {
-      const int b = (int)(sc & 1);
-      if (!mbar_wait(&s_full[b], (sc >> 1) & 1)) return false;
-      tc_fence_after();
-      return true;
-    };
-    auto release_s = [&]() {
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[sc & 1]);
-      ++sc;
-    };
     for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x, ++n_item) {
       int qt, hb, sb;
       decode(item, qt, hb, sb);
       const int nkv = qt + 1;
-      const int q = qt * kFaTile + r_in;                   // query index in the sequence
-      const bool row_ok = q < fp.L;
-      // zeros above the diagonal: this warp's rows, keys (qt + 1) * 128 .. L - 1
+      // zeros above the diagonal: keys (qt + 1) * 128 .. L - 1 of this warp's rows
       {
         const int c_begin = nkv * kFaTile;
         const int z = fp.L - c_begin;
         if (z > 0) {
-          for (int rr = 0; rr < 32; ++rr) {
+          for (int rr = half; rr < 32; rr += 2) {
             const int qq = qt * kFaTile + quarter * 32 + rr;
             if (qq >= fp.L) break;
             uint16_t* row = fp.P + (((int64_t)sb * fp.nh + hb) * fp.L + qq) * (int64_t)fp.L + c_begin;
@@ -320,85 +330,110 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           }
         }
       }
-      // pass 1: running maximum and sum of the row
+      // pass 1: this half's running maximum (log2 units) and sum of the row
       float m = -INFINITY, l = 0.0f;
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (!(ok = wait_s())) break;
-        const uint32_t t_s = t_lane + (uint32_t)((sc & 1) * kFaTile);
+      for (int j = 0; j < nkv && ok; ++j, ++sc) {
+        if ((j & 1) != half) continue;
+        const int b = (int)(sc & 1);
+        if (!(ok = mbar_wait(&s_full[b], (sc >> 1) & 1))) break;
+        tc_fence_after();
+        const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile);
         const bool diag = j == qt;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_s + c0, r);
+        for (int c0 = 0; c0 < kFaTile; c0 += 64) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld_32x32b_x32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_ld_wait();
-          float v[32];
           float mx = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            v[k] = (diag && c0 + k > r_in) ? -INFINITY : fp.alpha * __uint_as_float(r[k]);
-            mx = fmaxf(mx, v[k]);
+          for (int k = 0; k < 64; ++k) {
+            const float v = (diag && c0 + k > r_in) ? -INFINITY : al * __uint_as_float(r[k]);
+            r[k] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
           }
           const float m_new = fmaxf(m, mx);
-          float s = 0.0f;
+          float sum = 0.0f;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) s += __expf(v[k] - m_new);
-          l = (m == -INFINITY ? 0.0f : l * __expf(m - m_new)) + s;
+          for (int k = 0; k < 64; ++k) sum += ex2_approx(__uint_as_float(r[k]) - m_new);
+          l = (m == -INFINITY ? 0.0f : l * ex2_approx(m - m_new)) + sum;
           m = m_new;
         }
-        release_s();
-      }
-      const float inv = 1.0f / l;
-      // pass 2: P_j = exp(S_j - m) / l to shared memory (operand of O += P V) and to P
-      for (int j = 0; j < nkv && ok; ++j) {
-        if (!(ok = wait_s())) break;
-        const uint32_t t_s = t_lane + (uint32_t)((sc & 1) * kFaTile);
-        const int b = (int)(pc & 1);
-        // the buffer is free once the products that read it are done and this
-        // warp's store of it has read it
-        if (!(ok = mbar_wait(&p_empty[b], ((pc >> 1) & 1) ^ 1))) break;
-        if (lane == 0) bulk_wait_read<1>();
+        tc_fence_before();
         __syncwarp();
-        uint8_t* pbuf = sP + b * kFaPBytes;
+        if (lane == 0) mbar_arrive(&s_empty[b]);
+      }
+      if (!ok) break;
+      // merge the two halves (the same expression, in the same order, in both);
+      // the barrier also orders this item's P writes after every warp's O stores
+      // of the previous item have read the shared memory they reuse
+      if (lane == 0) bulk_wait_read<0>();
+      s_ml[(half * 128 + r_in) * 2] = m;
+      s_ml[(half * 128 + r_in) * 2 + 1] = l;
+      fa_softmax_sync();
+      const float m0 = s_ml[r_in * 2], l0 = s_ml[r_in * 2 + 1];
+      const float m1 = s_ml[(128 + r_in) * 2], l1 = s_ml[(128 + r_in) * 2 + 1];
+      m = fmaxf(m0, m1);
+      l = (m0 == -INFINITY ? 0.0f : l0 * ex2_approx(m0 - m)) + (m1 == -INFINITY ? 0.0f : l1 * ex2_approx(m1 - m));
+      const float inv = 1.0f / l;
+      // pass 2: P_j = exp(S_j - max) / sum to shared memory (operand of O += P V) and to P
+      for (int j = 0; j < nkv && ok; ++j, ++sc, ++pc) {
+        if ((j & 1) != half) continue;
+        const int b = (int)(sc & 1);
+        const int pb = (int)(pc & 1);
+        if (!(ok = mbar_wait(&s_full[b], (sc >> 1) & 1))) break;
+        tc_fence_after();
+        // the P buffer is free once the products that read it are done and this
+        // warp's store of its rows two tiles ago has read it
+        if (!(ok = mbar_wait(&p_empty[pb], ((pc >> 1) & 1) ^ 1))) break;
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile);
+        uint8_t* pbuf = sP + pb * kFaPBytes;
         const bool diag = j == qt;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(t_s + c0, r);
+        for (int c0 = 0; c0 < kFaTile; c0 += 64) {
+          uint32_t r[64];
+          tmem_ld_32x32b_x32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+          tmem_ld_32x32b_x32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
           tmem_ld_wait();
-          uint32_t pk[16];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const int k0 = 2 * k, k1 = 2 * k + 1;
-            const float p0 = (diag && c0 + k0 > r_in) ? 0.0f : __expf(fp.alpha * __uint_as_float(r[k0]) - m) * inv;
-            const float p1 = (diag && c0 + k1 > r_in) ? 0.0f : __expf(fp.alpha * __uint_as_float(r[k1]) - m) * inv;
-            pk[k] = pack_bf16x2(p0, p1);
-          }
-          // row r_in, keys c0 .. c0 + 31: chunks of 8 keys in the 128-byte swizzle of atom c0 / 64
+          // row r_in, keys c0 .. c0 + 63 = atom c0 / 64: 8 chunks of 8 keys in its 128-byte swizzle
           uint8_t* atom = pbuf + (c0 >> 6) * kFaAtomBytes + r_in * 128;
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int chunk = ((c0 & 63) >> 3) + g;
-            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r_in & 7)) << 4)) =
-                make_uint4(pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+          for (int g = 0; g < 8; ++g) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int k0 = 8 * g + 2 * k, k1 = k0 + 1;
+              const float p0 = (diag && c0 + k0 > r_in) ? 0.0f : ex2_approx(fmaf(__uint_as_float(r[k0]), al, -m)) * inv;
+              const float p1 = (diag && c0 + k1 > r_in) ? 0.0f : ex2_approx(fmaf(__uint_as_float(r[k1]), al, -m)) * inv;
+              pk[k] = pack_bf16x2(p0, p1);
+            }
+            *reinterpret_cast<uint4*>(atom + ((g ^ (r_in & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
         }
-        release_s();
+        tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
+          mbar_arrive(&s_empty[b]);
           for (int a = 0; a < 2; ++a)
             tma_store_4d(&mP, pbuf + a * kFaAtomBytes + quarter * 32 * 128, j * kFaTile + 64 * a,
                          qt * kFaTile + quarter * 32, hb, sb);
           bulk_commit();
-          mbar_arrive(&p_full[b]);
+          mbar_arrive(&p_full[pb]);
         }
-        ++pc;
       }
       if (!ok) break;
-      // O: the accumulator is final; bf16 through 32 x 32 boxes
+      // every warp's P stores have read the P buffers, which now stage O
+      if (lane == 0) bulk_wait_read<0>();
+      fa_softmax_sync();
       if (!(ok = mbar_wait(o_full, n_item & 1))) break;
       tc_fence_after();
-      for (int c0 = 0; c0 < fp.d_pad; c0 += 32) {
+      // O: the accumulator is final; bf16 through 32 x 32 boxes, the column blocks
+      // shared out between the halves, staged in the P buffers
+      uint8_t* my_o = sP + (warp - 2) * 2 * kFaOStageBytes;
+      for (int c0 = 32 * half; c0 < fp.d_pad; c0 += 64) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_lane + 256u + (uint32_t)c0, r);
         tmem_ld_wait();
@@ -426,7 +461,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(o_empty);
-      (void)row_ok;
     }
     if (!ok) record_status(status, kStatusTimeout, 23);
     if (lane == 0) bulk_wait_all();
