@@ -297,7 +297,11 @@ def attn_bench(wl, dev, stream, args):
     import torch
     from transformer_lm_megatron_gb300 import mlp
     from transformer_lm_megatron_gb300 import inputs as gin
-    c = gin.ATTN_MTNLG
+    c = dict(gin.ATTN_MTNLG)
+    if args.attn_h:
+        # the same head size (h / heads) and sequence at a smaller hidden size
+        c["nh"] = args.attn_h * c["nh"] // c["h"]
+        c["h"] = args.attn_h
     h, nh, t, L, T = c["h"], c["nh"], c["t"], c["seq_len"], c["tokens"]
     w, X, dOut = gin.make_attn_inputs(h, T, device=dev)
     buf = mlp.AttnBuffers(T, h, nh, L, device=dev)
@@ -305,10 +309,10 @@ def attn_bench(wl, dev, stream, args):
     def step():
         mlp.attn_step(h, nh, t, L, wl.p, wl.seed, w, X, dOut, buf, accumulate=False, stream=stream)
 
-    for _ in range(3):
+    for _ in range(max(args.warmup, 3) if args.attn_only else 3):
         step()
     torch.cuda.synchronize(dev)
-    n = 10
+    n = args.steps if args.attn_only else 10
     tr = mlp.Trace(capacity=40 * n)
     tr.start()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -412,6 +416,12 @@ def run_ours(args, wl, rank, world, dist):
     gb_build.build()
     mlp.load()
     mlp.mlp_set_tile_scheduler({"default": -1, "static": 0, "dynamic": 1}[args.tile_scheduler])
+    if args.attn_only:
+        # the attention block alone (the next row), e.g. for a counter capture of its kernels
+        out = attn_bench(wl, dev, torch.cuda.current_stream(dev), args)
+        if rank == 0:
+            print(json.dumps({"attn_block": out}), flush=True)
+        return
 
     weights = gin.make_weights(wl.h, wl.ffn, device=dev)
     mbs = [gin.make_microbatch(wl.tokens, wl.h, j, device=dev) for j in range(wl.k)]
@@ -717,6 +727,10 @@ def main():
     ap.add_argument("--no-adam", action="store_true", help="skip the Adam-step measurement")
     ap.add_argument("--no-attn", action="store_true", help="skip the attention-block measurement")
     ap.add_argument("--no-others", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--attn-only", action="store_true",
+                    help="time only the attention block (--steps timed, --warmup untimed steps)")
+    ap.add_argument("--attn-h", type=int, default=0,
+                    help="hidden size of the attention block (default 20480; the head size stays 160)")
     ap.add_argument("--tile-scheduler", default="default", choices=["default", "dynamic", "static"],
                     help="order in which the GEMMs hand out output tiles (results are bit-identical): "
                          "default = dynamic for the batched attention products only")
