@@ -317,19 +317,6 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       int qt, hb, sb;
       decode(item, qt, hb, sb);
       const int nkv = qt + 1;
-      // zeros above the diagonal: keys (qt + 1) * 128 .. L - 1 of this warp's rows
-      {
-        const int c_begin = nkv * kFaTile;
-        const int z = fp.L - c_begin;
-        if (z > 0) {
-          for (int rr = half; rr < 32; rr += 2) {
-            const int qq = qt * kFaTile + quarter * 32 + rr;
-            if (qq >= fp.L) break;
-            uint16_t* row = fp.P + (((int64_t)sb * fp.nh + hb) * fp.L + qq) * (int64_t)fp.L + c_begin;
-            for (int c = lane * 8; c < z; c += 256) *reinterpret_cast<uint4*>(row + c) = make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
       // pass 1: this half's running maximum (log2 units) and sum of the row
       float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nkv && ok; ++j, ++sc) {
@@ -339,15 +326,17 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         tc_fence_after();
         const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile);
         const bool diag = j == qt;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kFaTile; c0 += 64) {
-          uint32_t r[64];
-          tmem_ld_32x32b_x32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld_32x32b_x32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          tmem_ld_wait();
+        // 32-column blocks, the next block's TMEM load in flight while this one is processed
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(t_s, ra);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
+          uint32_t (&r)[32] = (c0 & 32) ? rb : ra;
+          if (c0 + 32 < kFaTile) tmem_ld_32x32b_x32(t_s + c0 + 32, (c0 & 32) ? ra : rb);
           float mx = -INFINITY;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) {
+          for (int k = 0; k < 32; ++k) {
             const float v = (diag && c0 + k > r_in) ? -INFINITY : al * __uint_as_float(r[k]);
             r[k] = __float_as_uint(v);
             mx = fmaxf(mx, v);
@@ -355,9 +344,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           const float m_new = fmaxf(m, mx);
           float sum = 0.0f;
 #pragma unroll
-          for (int k = 0; k < 64; ++k) sum += ex2_approx(__uint_as_float(r[k]) - m_new);
+          for (int k = 0; k < 32; ++k) sum += ex2_approx(__uint_as_float(r[k]) - m_new);
           l = (m == -INFINITY ? 0.0f : l * ex2_approx(m - m_new)) + sum;
           m = m_new;
+          tmem_ld_wait();
         }
         tc_fence_before();
         __syncwarp();
@@ -391,16 +381,17 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile);
         uint8_t* pbuf = sP + pb * kFaPBytes;
         const bool diag = j == qt;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kFaTile; c0 += 64) {
-          uint32_t r[64];
-          tmem_ld_32x32b_x32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-          tmem_ld_32x32b_x32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-          tmem_ld_wait();
-          // row r_in, keys c0 .. c0 + 63 = atom c0 / 64: 8 chunks of 8 keys in its 128-byte swizzle
+        uint32_t ra[32], rb[32];
+        tmem_ld_32x32b_x32(t_s, ra);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
+          uint32_t (&r)[32] = (c0 & 32) ? rb : ra;
+          if (c0 + 32 < kFaTile) tmem_ld_32x32b_x32(t_s + c0 + 32, (c0 & 32) ? ra : rb);
+          // row r_in, keys c0 .. c0 + 31: 4 chunks of 8 keys in the 128-byte swizzle of atom c0 / 64
           uint8_t* atom = pbuf + (c0 >> 6) * kFaAtomBytes + r_in * 128;
 #pragma unroll
-          for (int g = 0; g < 8; ++g) {
+          for (int g = 0; g < 4; ++g) {
             uint32_t pk[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -409,8 +400,10 @@ __global__ void __launch_bounds__(kFaThreads, 1)
               const float p1 = (diag && c0 + k1 > r_in) ? 0.0f : ex2_approx(fmaf(__uint_as_float(r[k1]), al, -m)) * inv;
               pk[k] = pack_bf16x2(p0, p1);
             }
-            *reinterpret_cast<uint4*>(atom + ((g ^ (r_in & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            const int chunk = ((c0 & 63) >> 3) + g;
+            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r_in & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           }
+          tmem_ld_wait();
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -425,6 +418,20 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         }
       }
       if (!ok) break;
+      // zeros above the diagonal: keys (qt + 1) * 128 .. L - 1 of this warp's rows
+      // (while the last O += P V runs)
+      {
+        const int c_begin = nkv * kFaTile;
+        const int z = fp.L - c_begin;
+        if (z > 0) {
+          for (int rr = half; rr < 32; rr += 2) {
+            const int qq = qt * kFaTile + quarter * 32 + rr;
+            if (qq >= fp.L) break;
+            uint16_t* row = fp.P + (((int64_t)sb * fp.nh + hb) * fp.L + qq) * (int64_t)fp.L + c_begin;
+            for (int c = lane * 8; c < z; c += 256) *reinterpret_cast<uint4*>(row + c) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
       // every warp's P stores have read the P buffers, which now stage O
       if (lane == 0) bulk_wait_read<0>();
       fa_softmax_sync();
