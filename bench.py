@@ -246,7 +246,9 @@ def other_workloads(dev, stream, steps=5, warmup=2):
     """fwd+bwd TFLOP/s of the smaller named workloads, each step being all of its
     micro-batches (the first writes the gradients, the rest add).  The sweep runs
     one slice per call, as its workload description says; the others all slices
-    per call."""
+    per call.  Each step is timed as issued (eager) and as the replay of a CUDA graph
+    captured from it: the library keeps no per-call host state that a replay would
+    miss, and its device-side counters return to zero after every kernel."""
     import torch
     from transformer_lm_megatron_gb300 import inputs as gin
     from transformer_lm_megatron_gb300 import mlp
@@ -258,10 +260,10 @@ def other_workloads(dev, stream, steps=5, warmup=2):
         mbs = [gin.make_microbatch(w.tokens, w.h, j, device=dev) for j in range(min(w.k, 4))]
         buf = mlp.BlockBuffers(w.tokens, w.h, w.ffn, w.t, device=dev)
 
-        def step():
+        def step(s=stream):
             for j in range(w.k):
                 X, dO = mbs[j % len(mbs)]
-                mlp.block_step(w, weights, X, dO, buf, token_offset=j * w.tokens, slice_mode=mode, stream=stream,
+                mlp.block_step(w, weights, X, dO, buf, token_offset=j * w.tokens, slice_mode=mode, stream=s,
                                accumulate=j > 0)
 
         for _ in range(warmup):
@@ -275,8 +277,25 @@ def other_workloads(dev, stream, steps=5, warmup=2):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         ms = e0.elapsed_time(e1) / steps
+        # the same step captured once and replayed
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(torch.cuda.current_stream(dev))
+        for _ in range(warmup):
+            graph.replay()
+        torch.cuda.synchronize(dev)
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        g0.record()
+        for _ in range(steps):
+            graph.replay()
+        g1.record()
+        torch.cuda.synchronize(dev)
+        gms = g0.elapsed_time(g1) / steps
+        del graph
         out[name] = {"tokens": w.tokens, "h": w.h, "ffn": w.ffn, "t": w.t, "micro_batches": w.k,
-                     "slice_calls": mode, "ms_per_step": ms, "TFLOPs": w.flops_total() / (ms / 1e3) / 1e12}
+                     "slice_calls": mode, "ms_per_step": ms, "TFLOPs": w.flops_total() / (ms / 1e3) / 1e12,
+                     "graph_ms_per_step": gms, "graph_TFLOPs": w.flops_total() / (gms / 1e3) / 1e12}
         del weights, mbs, buf
     if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
         raise RuntimeError(mlp.last_error())

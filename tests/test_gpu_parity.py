@@ -404,3 +404,35 @@ def test_tile_scheduler_changes_no_bit(tokens, h, ffn, t, mode, cta_pair_mode, t
         assert torch.equal(g_dy2[k], g_st[k]), k
     r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
     compare_full(s, [o_dy[-1]], g_dy, [r_outs[-1]], r_grads, label="dynamic tile order")
+
+
+@pytest.mark.parametrize("mode", ["all", "each"])
+def test_cuda_graph_replay_equals_eager(mode):
+    """A step captured in a CUDA graph and replayed gives, bit for bit, what the
+    eager calls give, replay after replay: the library keeps no per-call host state
+    that a replay would miss, and its device-side counters (split tail, tile order)
+    return to zero after every kernel."""
+    s = Shape(tokens=512, h=1280, ffn=2048, t=2, k=2)     # F2 and B5 split their tail
+    w_dev, mbs_dev, _, _ = make_case(s)
+    o_ref, g_ref = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, reset=False, first_overwrites=True)
+    buf = mlp.BlockBuffers(s.tokens, s.h, s.ffn, s.t)
+
+    def step():
+        for j, (X, dO) in enumerate(mbs_dev):
+            mlp.block_step(s, w_dev, X, dO, buf, token_offset=j * s.tokens, slice_mode=mode, accumulate=j > 0)
+
+    step()                                    # first calls on this shape happen outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        for k in ("dA", "da", "dB", "db", "O", "dX"):
+            getattr(buf, k).fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+        for k in ("O", "dX", "U", "Y", "dU", "dZ"):
+            assert torch.equal(getattr(buf, k).cpu(), o_ref[-1][k]), k
+        for k in ("dA", "da", "dB", "db"):
+            assert torch.equal(getattr(buf, k).cpu(), g_ref[k]), k
