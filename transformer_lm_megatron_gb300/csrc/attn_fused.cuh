@@ -481,3 +481,360 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 }
 
 }  // namespace gbmlp
+
+namespace gbmlp {
+
+// ---------------------------------------------------------------------------
+// Fused causal attention core of the backward, per (sequence, head) and tile j of
+// 128 keys, over the query tiles i = j .. last (the keys of tile j see only those):
+//
+//   dP^T = V_j dO_i^T                      (tensor memory)
+//   dV_j += P_ij^T dO_i                    (tensor memory, fp32)
+//   dS^T = P_ij^T (dP^T - delta_i) / sqrt(d), bf16, one key row per thread
+//   dK_j += dS^T Q_i                       (tensor memory, fp32)
+//
+// with delta_i = rowsum(dO_i * O_i) given (k_attn_delta), the stored bf16 P of the
+// forward, and dS^T written to global memory for dQ = dS K (a batched GEMM that
+// reads it as an MN-major operand).  dK_j and dV_j go to dQKV in bf16.
+// Every operand tile is loaded once, as 64-column swizzle atoms of 128 rows: such
+// an atom is also two stacked MN-major chunks of 64 rows, so the same bytes serve
+// as a K-major operand (dP^T, dK's A) and as an MN-major one (dV's A and B, dK's B).
+// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-5 one key row per thread.
+// TMEM: dV at columns 0.., dK at 192.., dP^T at 384 .. 511.
+// ---------------------------------------------------------------------------
+constexpr int kFbThreads = 64 + 32 * 4;
+constexpr size_t kFbSmemBytes = (size_t)kFaTileBytes * 3 /* V, dO, Q */ + 2 * kFaPBytes /* P, dS^T */ +
+                                kFaTile * sizeof(float) /* delta */ + 1024 /*align*/ + 256 /*barriers*/;
+static_assert(kFbSmemBytes <= 232448, "smem budget");
+
+struct FbParams {
+  int L, nh, ns, d, d_pad, n_atoms;
+  float alpha;     // 1 / sqrt(d)
+  uint16_t* dST;   // [ns, nh, L keys, L queries] bf16: dS transposed
+};
+
+__global__ void __launch_bounds__(kFbThreads, 1)
+    k_attn_bwd_fused(const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mQ,
+                     const __grid_constant__ CUtensorMap mdO, const __grid_constant__ CUtensorMap mP,
+                     const __grid_constant__ CUtensorMap mDelta, const __grid_constant__ CUtensorMap mDS,
+                     const __grid_constant__ CUtensorMap mdK, const __grid_constant__ CUtensorMap mdV, FbParams fp,
+                     int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sV = smem;
+  uint8_t* sdO = sV + kFaTileBytes;
+  uint8_t* sQ = sdO + kFaTileBytes;
+  uint8_t* sP = sQ + kFaTileBytes;
+  uint8_t* sDS = sP + kFaPBytes;
+  float* sDelta = reinterpret_cast<float*>(sDS + kFaPBytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sDelta + kFaTile);
+  uint64_t* v_full = bar + 0;
+  uint64_t* v_empty = bar + 1;
+  uint64_t* do_full = bar + 2;
+  uint64_t* do_empty = bar + 3;
+  uint64_t* q_full = bar + 4;
+  uint64_t* q_empty = bar + 5;
+  uint64_t* p_full = bar + 6;
+  uint64_t* p_empty = bar + 7;
+  uint64_t* dp_full = bar + 8;
+  uint64_t* dp_empty = bar + 9;
+  uint64_t* ds_full = bar + 10;
+  uint64_t* ds_empty = bar + 11;
+  uint64_t* acc_full = bar + 12;
+  uint64_t* acc_empty = bar + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 14);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_t = (fp.L + kFaTile - 1) / kFaTile;   // query tiles = key tiles
+  const int heads = fp.nh * fp.ns;
+  const int num_items = n_t * heads;
+  const uint32_t tile_tx = (uint32_t)fp.n_atoms * kFaAtomBytes;
+
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) {
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    mbar_init(do_full, 1);
+    mbar_init(do_empty, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(p_full, 1);
+    mbar_init(p_empty, 1 + 4);   // the products that read P, and the 4 warps that read it
+    mbar_init(dp_full, 1);
+    mbar_init(dp_empty, 4);
+    mbar_init(ds_full, 4);
+    mbar_init(ds_empty, 1);
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&mV);
+    tma_prefetch_desc(&mQ);
+    tma_prefetch_desc(&mdO);
+    tma_prefetch_desc(&mP);
+    tma_prefetch_desc(&mDelta);
+    tma_prefetch_desc(&mDS);
+    tma_prefetch_desc(&mdK);
+    tma_prefetch_desc(&mdV);
+  }
+  if (warp == 1) {
+    tmem_alloc<false>(tmem_slot, kFaTmemCols);
+    tmem_relinquish<false>();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  if (threadIdx.x == 0) s_skip = (status != nullptr && *reinterpret_cast<volatile int*>(status) != 0) ? 1 : 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int item_end = s_skip ? 0 : num_items;
+
+  // item -> (key tile, head, sequence): the key tiles that see the most query tiles first
+  auto decode = [&](int item, int& kt, int& hb, int& sb) {
+    kt = item / heads;
+    const int r = item % heads;
+    hb = r % fp.nh;
+    sb = r / fp.nh;
+  };
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t nv = 0, ndo = 0, np = 0, nq = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x) {
+        int kt, hb, sb;
+        decode(item, kt, hb, sb);
+        if (!(ok = mbar_wait(v_empty, (nv & 1) ^ 1))) break;
+        mbar_arrive_expect_tx(v_full, tile_tx);
+        for (int a = 0; a < fp.n_atoms; ++a) tma_load_4d(sV + a * kFaAtomBytes, &mV, v_full, 64 * a, kt * kFaTile, hb, sb);
+        ++nv;
+        for (int i = kt; i < n_t && ok; ++i) {
+          if (!(ok = mbar_wait(do_empty, (ndo & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(do_full, tile_tx);
+          for (int a = 0; a < fp.n_atoms; ++a)
+            tma_load_4d(sdO + a * kFaAtomBytes, &mdO, do_full, 64 * a, i * kFaTile, hb, sb);
+          ++ndo;
+          if (!(ok = mbar_wait_cluster(p_empty, (np & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(p_full, kFaPBytes + kFaTile * sizeof(float));
+          for (int a = 0; a < 2; ++a)
+            tma_load_4d(sP + a * kFaAtomBytes, &mP, p_full, kt * kFaTile + 64 * a, i * kFaTile, hb, sb);
+          tma_load_2d(sDelta, &mDelta, p_full, i * kFaTile, sb * fp.nh + hb, 0, false);
+          ++np;
+          if (!(ok = mbar_wait(q_empty, (nq & 1) ^ 1))) break;
+          mbar_arrive_expect_tx(q_full, tile_tx);
+          for (int a = 0; a < fp.n_atoms; ++a) tma_load_4d(sQ + a * kFaAtomBytes, &mQ, q_full, 64 * a, i * kFaTile, hb, sb);
+          ++nq;
+        }
+      }
+      if (!ok) record_status(status, kStatusTimeout, 30);
+      // drain: every copy issued has landed before the CTA may exit
+      if (nv > 0 && !mbar_wait(v_full, (nv - 1) & 1)) record_status(status, kStatusTimeout, 31);
+      if (ndo > 0 && !mbar_wait(do_full, (ndo - 1) & 1)) record_status(status, kStatusTimeout, 31);
+      if (np > 0 && !mbar_wait(p_full, (np - 1) & 1)) record_status(status, kStatusTimeout, 31);
+      if (nq > 0 && !mbar_wait(q_full, (nq - 1) & 1)) record_status(status, kStatusTimeout, 31);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc_dp = make_idesc_bf16(kFaTile, kFaTile, false, false);
+      const uint32_t idesc_dv = make_idesc_bf16(kFaTile, fp.d_pad, true, true);
+      const uint32_t idesc_dk = make_idesc_bf16(kFaTile, fp.d_pad, false, true);
+      const int nk_d = fp.d_pad / 16;
+      const uint32_t t_dv = tmem_base, t_dk = tmem_base + 192u, t_dp = tmem_base + 384u;
+      uint32_t nv = 0, ndo = 0, np = 0, nq = 0, ndp = 0, nds = 0, n_item = 0;
+      bool ok = true;
+      auto issue_dp = [&]() -> bool {  // dP^T = V dO^T
+        if (!mbar_wait(do_full, ndo & 1) || !mbar_wait(dp_empty, (ndp & 1) ^ 1)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(sV), ob = smem_u32(sdO);
+        for (int kk = 0; kk < nk_d; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kFaAtomBytes + (uint32_t)(kk & 3) * 32;
+          umma_bf16(t_dp, make_sdesc_sw128(vb + off, 16, 1024), make_sdesc_sw128(ob + off, 16, 1024), idesc_dp,
+                    kk > 0 ? 1u : 0u);
+        }
+        umma_commit(dp_full);
+        ++ndp;
+        return true;
+      };
+      auto issue_dv = [&](bool first) -> bool {  // dV += P^T dO
+        if (!mbar_wait(p_full, np & 1)) return false;
+        tc_fence_after();
+        const uint32_t pb = smem_u32(sP), ob = smem_u32(sdO);
+        for (int kk = 0; kk < kFaTile / 16; ++kk)
+          umma_bf16(t_dv, make_sdesc_sw128(pb + kk * 2048, kFaAtomBytes, 1024),
+                    make_sdesc_sw128(ob + kk * 2048, kFaAtomBytes, 1024), idesc_dv, (first && kk == 0) ? 0u : 1u);
+        umma_commit(do_empty);
+        umma_commit(p_empty);
+        ++ndo;
+        ++np;
+        return true;
+      };
+      auto issue_dk = [&](bool first) -> bool {  // dK += dS^T Q
+        if (!mbar_wait(ds_full, nds & 1) || !mbar_wait(q_full, nq & 1)) return false;
+        tc_fence_after();
+        const uint32_t sb_ = smem_u32(sDS), qb = smem_u32(sQ);
+        for (int kk = 0; kk < kFaTile / 16; ++kk) {
+          const uint32_t off = (uint32_t)(kk >> 2) * kFaAtomBytes + (uint32_t)(kk & 3) * 32;
+          umma_bf16(t_dk, make_sdesc_sw128(sb_ + off, 16, 1024), make_sdesc_sw128(qb + kk * 2048, kFaAtomBytes, 1024),
+                    idesc_dk, (first && kk == 0) ? 0u : 1u);
+        }
+        umma_commit(q_empty);
+        umma_commit(ds_empty);
+        ++nq;
+        ++nds;
+        return true;
+      };
+      for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x, ++n_item) {
+        int kt, hb, sb;
+        decode(item, kt, hb, sb);
+        if (!(ok = mbar_wait(v_full, nv & 1))) break;
+        ++nv;
+        // the previous item's dK and dV have been read out of tensor memory
+        if (!(ok = mbar_wait(acc_empty, (n_item & 1) ^ 1))) break;
+        tc_fence_after();
+        ok = issue_dp() && issue_dv(true);
+        for (int i = kt + 1; i < n_t && ok; ++i) ok = issue_dp() && issue_dk(i - 1 == kt) && issue_dv(false);
+        if (ok) ok = issue_dk(n_t - 1 == kt);
+        if (ok) {
+          umma_commit(v_empty);
+          umma_commit(acc_full);
+        }
+      }
+      if (!ok) record_status(status, kStatusTimeout, 32);
+    }
+  } else {
+    // -------------------------------------------------------------- one key row per thread
+    const int quarter = warp & 3;
+    const int k_in = quarter * 32 + lane;                 // key row within the tile
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    uint32_t np = 0, ndp = 0, nds = 0, n_out = 0, n_item = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < item_end && ok; item += gridDim.x, ++n_item) {
+      int kt, hb, sb;
+      decode(item, kt, hb, sb);
+      for (int i = kt; i < n_t && ok; ++i) {
+        // dP^T row of key k_in, queries 0 .. 127 of tile i
+        if (!(ok = mbar_wait(dp_full, ndp & 1))) break;
+        tc_fence_after();
+        uint32_t dp[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_lane + 384u + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&dp[32 * c]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dp_empty);
+        ++ndp;
+        // P (and delta) of tile (i, kt); the dS^T buffer free: dK's product read it,
+        // and this warp's store of it has read it
+        if (!(ok = mbar_wait(p_full, np & 1))) break;
+        if (!(ok = mbar_wait(ds_empty, (nds & 1) ^ 1))) break;
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+        // P[q][k_in] sits in row q of atom k_in / 64, 16-byte chunk ((k_in % 64) / 8) ^ (q % 8)
+        const uint8_t* pcol = sP + (k_in >> 6) * kFaAtomBytes + (k_in & 7) * 2;
+        const int pchunk = (k_in & 63) >> 3;
+        uint8_t* dsrow = sDS + k_in * 128;
+#pragma unroll
+        for (int g = 0; g < 16; ++g) {          // queries 8 g .. 8 g + 7
+          uint32_t pk[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float v2[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int q = 8 * g + 2 * e + u;
+              const uint16_t pbits = *reinterpret_cast<const uint16_t*>(pcol + q * 128 + ((pchunk ^ (q & 7)) << 4));
+              const float p = __uint_as_float((uint32_t)pbits << 16);
+              v2[u] = p * (__uint_as_float(dp[q]) - sDelta[q]) * fp.alpha;
+            }
+            pk[e] = pack_bf16x2(v2[0], v2[1]);
+          }
+          // dS^T row k_in, queries 8 g ..: atom g / 8, chunk (g % 8) ^ (k_in % 8)
+          *reinterpret_cast<uint4*>(dsrow + (g >> 3) * kFaAtomBytes + (((g & 7) ^ (k_in & 7)) << 4)) =
+              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(p_empty);
+          for (int a = 0; a < 2; ++a)
+            tma_store_4d(&mDS, sDS + a * kFaAtomBytes + quarter * 32 * 128, i * kFaTile + 64 * a,
+                         kt * kFaTile + quarter * 32, hb, sb);
+          bulk_commit();
+          mbar_arrive(ds_full);
+        }
+        ++np;
+        ++nds;
+      }
+      if (!ok) break;
+      // dS^T tile (key tile kt, query tile kt - 1) lies above the diagonal; the dQ
+      // product of the 256-query tile that holds query tile kt - 1 reads it when kt
+      // is odd, so it must hold zeros
+      if (kt & 1) {
+        for (int rr = 0; rr < 32; rr += 2) {
+          const int key = kt * kFaTile + quarter * 32 + rr + (lane >> 4);
+          if (key < fp.L) {
+            uint16_t* row = fp.dST + (((int64_t)sb * fp.nh + hb) * fp.L + key) * (int64_t)fp.L + (kt - 1) * kFaTile;
+            *reinterpret_cast<uint4*>(row + (lane & 15) * 8) = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      // dV and dK: bf16 through 32 x 32 boxes staged in this warp's own rows of the
+      // dS^T buffer (its last store and dK's last product have read them)
+      if (!(ok = mbar_wait(acc_full, n_item & 1))) break;
+      tc_fence_after();
+      if (lane == 0) bulk_wait_read<0>();
+      __syncwarp();
+      uint8_t* my_o = sDS + quarter * 32 * 128;   // 4 KB: two boxes
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t col0 = which == 0 ? 0u : 192u;
+        const CUtensorMap* map = which == 0 ? &mdV : &mdK;
+        for (int c0 = 0; c0 < fp.d_pad; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_lane + col0 + (uint32_t)c0, r);
+          tmem_ld_wait();
+          if (c0 >= fp.d) continue;
+          uint8_t* box = my_o + (n_out & 1) * kFaOStageBytes;
+          if (lane == 0) bulk_wait_read<1>();
+          __syncwarp();
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t off = lane * 64 + ((g ^ ((lane >> 1) & 3)) << 4);
+            *reinterpret_cast<uint4*>(box + off) =
+                make_uint4(pack_bf16x2(__uint_as_float(r[8 * g]), __uint_as_float(r[8 * g + 1])),
+                           pack_bf16x2(__uint_as_float(r[8 * g + 2]), __uint_as_float(r[8 * g + 3])),
+                           pack_bf16x2(__uint_as_float(r[8 * g + 4]), __uint_as_float(r[8 * g + 5])),
+                           pack_bf16x2(__uint_as_float(r[8 * g + 6]), __uint_as_float(r[8 * g + 7])));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(map, box, c0, kt * kFaTile + quarter * 32, hb, sb);
+            bulk_commit();
+          }
+          ++n_out;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        bulk_wait_read<0>();   // the staged boxes have been read before the next dS^T rows land there
+        mbar_arrive(acc_empty);
+      }
+    }
+    if (!ok) record_status(status, kStatusTimeout, 33);
+    if (lane == 0) bulk_wait_all();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<false>(tmem_base, kFaTmemCols);
+  }
+}
+
+}  // namespace gbmlp

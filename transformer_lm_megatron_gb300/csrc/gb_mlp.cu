@@ -113,6 +113,7 @@ struct DeviceState {
   int split_regions_used = 0;
   bool gemm_attr[32] = {};  // per GEMM instantiation: dynamic smem attribute set
   bool fa_attr = false;     // fused attention core: dynamic smem attribute set
+  bool fb_attr = false;     // fused attention backward core: dynamic smem attribute set
   int max_pairs[32] = {};   // per CTA-pair instantiation: co-resident clusters of two
 };
 
@@ -544,6 +545,66 @@ int attn_core_fused(DeviceState* st, const uint16_t* QKV, uint16_t* P, uint16_t*
   return launch_check(e, "fused attention core");
 }
 
+// The fused attention core of the backward: dK and dV into dQKV, dS^T into dST
+// (P's shape, keys x queries); delta = rowsum(dO * O) must be in `delta`.
+int attn_core_bwd_fused(DeviceState* st, const uint16_t* QKV, const uint16_t* P, const uint16_t* dO,
+                        const float* delta, uint16_t* dST, uint16_t* dQKV, int h, int nh, int L, int ns,
+                        cudaStream_t s) {
+  const int d = h / nh;
+  const int64_t h3 = 3 * (int64_t)h, LL = (int64_t)L * L;
+  FbParams fb;
+  fb.L = L;
+  fb.nh = nh;
+  fb.ns = ns;
+  fb.d = d;
+  fb.d_pad = (d + 15) & ~15;
+  fb.n_atoms = (fb.d_pad + 63) / 64;
+  fb.alpha = 1.0f / std::sqrt((float)d);
+  fb.dST = dST;
+  CUtensorMap mV, mQ, mdO, mP, mDelta, mDS, mdK, mdV;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
+  const auto l2 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
+  int rc = make_map4(&mV, bf, 2, QKV + 2 * h, d, L, h3, nh, d, ns, L * h3, 64, kFaTile, sw128, l2);
+  if (!rc) rc = make_map4(&mQ, bf, 2, QKV, d, L, h3, nh, d, ns, L * h3, 64, kFaTile, sw128, l2);
+  if (!rc) rc = make_map4(&mdO, bf, 2, dO, d, L, h, nh, d, ns, (int64_t)L * h, 64, kFaTile, sw128, l2);
+  if (!rc) rc = make_map4(&mP, bf, 2, P, L, L, L, nh, LL, ns, nh * LL, 64, kFaTile, sw128, l2);
+  if (!rc)
+    rc = make_map4(&mDS, bf, 2, dST, L, L, L, nh, LL, ns, nh * LL, 64, 32, sw128, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (!rc)
+    rc = make_map4(&mdK, bf, 2, dQKV + h, d, L, h3, nh, d, ns, L * h3, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (!rc)
+    rc = make_map4(&mdV, bf, 2, dQKV + 2 * h, d, L, h3, nh, d, ns, L * h3, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE);
+  if (rc) return rc;
+  {
+    // delta: fp32 [ns * nh rows][L], one 128-query box per load (zero past L)
+    cuuint64_t dims[2] = {(cuuint64_t)L, (cuuint64_t)ns * nh};
+    cuuint64_t strides[1] = {(cuuint64_t)L * 4};
+    cuuint32_t box[2] = {(cuuint32_t)kFaTile, 1};
+    cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(&mDelta, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(delta), dims, strides,
+                                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(MLP_ECUDA, "cuTensorMapEncodeTiled (softmax-gradient row sums) failed (%d)", (int)r);
+  }
+  if (!st->fb_attr) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(k_attn_bwd_fused, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFbSmemBytes);
+    if (e != cudaSuccess)
+      return fail(MLP_ECUDA, "cudaFuncSetAttribute (fused attention backward): %s", cudaGetErrorString(e));
+    st->fb_attr = true;
+  }
+  const int64_t items = (int64_t)((L + kFaTile - 1) / kFaTile) * nh * ns;
+  const unsigned grid = (unsigned)(items < st->sms ? items : st->sms);
+  const int ts = trace_pre(s);
+  const cudaError_t e = launch_kernel(k_attn_bwd_fused, dim3(grid), dim3(kFbThreads), kFbSmemBytes, s, 1, 1, mV, mQ,
+                                      mdO, mP, mDelta, mDS, mdK, mdV, fb, st->status);
+  trace_post(ts, s, kTraceAttnCore, (int64_t)ns * nh * L, L, d);
+  return launch_check(e, "fused attention backward core");
+}
+
 int softmax_launch(DeviceState* st, const float* S, uint16_t* P, int64_t rows, int cols, cudaStream_t s) {
   int64_t blocks = rows < (int64_t)st->sms * 16 ? rows : (int64_t)st->sms * 16;
   const int ts = trace_pre(s);
@@ -700,10 +761,31 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   ed.out0 = dO;
   rc = gemm(st, dZ, false, h, Wo, false, h, T, h, h, ed, s, kTraceAttnGemm);
   if (rc) return rc;
-  // per (sequence, head): dV = P^T dO, dS = P (dO V^T - delta) / sqrt(d) with delta = rowsum(dO * O)
-  // (fused: the product dO V^T never leaves the GEMM), dQ = dS K, dK = dS^T Q
   EpiParams est{};
   est.kind = kEpiStore;
+  if (g_attn_fused.load(std::memory_order_relaxed) && ((d + 15) & ~15) <= kFaMaxAtoms * 64) {
+    // delta = rowsum(dO * O); then, fused per (sequence, head, key tile): dV and dK,
+    // and dS^T for dQ = dS K (a batched GEMM reading dS^T as an MN-major operand)
+    float* delta = dP;
+    {
+      const int64_t warps = tokens * nh;
+      int64_t blocks = (warps + kDeltaWarps - 1) / kDeltaWarps;
+      if (blocks > (int64_t)st->sms * 16) blocks = (int64_t)st->sms * 16;
+      const int ts = trace_pre(s);
+      const cudaError_t e = launch_kernel(k_attn_delta, dim3((unsigned)blocks), dim3(kDeltaWarps * 32), 0, s, 1, 1,
+                                          (const uint16_t*)dO, (const uint16_t*)O, delta, tokens, h, nh, L);
+      trace_post(ts, s, kTraceSoftmax, tokens, h, 0);
+      rc = launch_check(e, "softmax-gradient row sums");
+      if (rc) return rc;
+    }
+    rc = attn_core_bwd_fused(st, QKV, P, dO, delta, dS, dQKV, h, nh, L, ns, s);
+    if (rc) return rc;
+    rc = gemm_batched(st, {dS, true, L, L, L, LL, nh * LL}, {QKV + h, true, d, L, h3, d, L * h3},
+                      {dQKV, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKUpTo);
+    if (rc) return rc;
+  } else {
+  // per (sequence, head): dV = P^T dO, dS = P (dO V^T - delta) / sqrt(d) with delta = rowsum(dO * O)
+  // (fused: the product dO V^T never leaves the GEMM), dQ = dS K, dK = dS^T Q
   rc = gemm_batched(st, {P, true, L, L, L, LL, nh * LL}, {dO, true, d, L, h, d, (int64_t)L * h},
                     {dQKV + 2 * h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKFrom);
   if (rc) return rc;
@@ -734,6 +816,7 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   rc = gemm_batched(st, {dS, true, L, L, L, LL, nh * LL}, {QKV, true, d, L, h3, d, L * h3},
                     {dQKV + h, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKFrom);
   if (rc) return rc;
+  }
   // dbqkv (+)= sum dQKV; dWqkv (+)= X^T dQKV; dX = [dOut +] dQKV Wqkv^T
   {
     const int ts = trace_pre(s);
