@@ -188,8 +188,8 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
  *   dX = [dOut +] dQKV Wqkv^T   (operator f; residual_grad selects the dOut term)
  * rowsum(dP P) is taken as rowsum(dO * O), the same quantity (P V = O), and dP is
  * never stored: the product dO V^T goes straight into dS in the GEMM's epilogue.
- * dZ, dO [tokens, h] and dS (P's shape) are bf16 workspaces (dS holds the softmax
- * gradient in a layout of the library's choosing, written only where it is read back),
+ * dZ, dO [tokens, h] and dS (P's shape) are bf16 workspaces (dS is written only in
+ * the tiles on or below the causal diagonal that are read back),
  * dP an fp32 workspace of at least n_seq * nh * seq_len floats (the row sums),
  * dQKV [tokens, 3h] bf16, dX [tokens, h] bf16.  Returns MLP_OK or an error.
  */
@@ -271,9 +271,8 @@ int mlp_set_split_tail(int enable);
  *     the key tiles, the first for each row's maximum and sum, the second writing
  *     the normalised bf16 P and accumulating O = P V; the S workspace is not used.
  *   forward, unfused: a batched GEMM writing S, the row softmax, a batched GEMM.
- *   backward, fused: per key tile, dP^T = V dO^T, dV += P^T dO, dS^T and dK +=
- *     dS^T Q in one kernel (dS is stored transposed in the dS workspace), then
- *     dQ = dS K as a batched GEMM.
+ *   backward, fused: per key tile, dP = dO V^T, dV += P^T dO, dS and dK += dS^T Q
+ *     in one kernel, then dQ = dS K as a batched GEMM.
  *   backward, unfused: batched GEMMs for dV, dO V^T (with the dS epilogue), dQ, dK.
  * The two agree within a bf16 rounding step of P (the softmax sums run in another
  * order).  Returns MLP_OK or MLP_EINVAL.

@@ -488,19 +488,20 @@ namespace gbmlp {
 // Fused causal attention core of the backward, per (sequence, head) and tile j of
 // 128 keys, over the query tiles i = j .. last (the keys of tile j see only those):
 //
-//   dP^T = V_j dO_i^T                      (tensor memory)
+//   dP = dO_i V_j^T                        (tensor memory, a query row per lane)
 //   dV_j += P_ij^T dO_i                    (tensor memory, fp32)
-//   dS^T = P_ij^T (dP^T - delta_i) / sqrt(d), bf16, one key row per thread
+//   dS = P_ij (dP - delta_i) / sqrt(d), bf16, one query row per thread
 //   dK_j += dS^T Q_i                       (tensor memory, fp32)
 //
 // with delta_i = rowsum(dO_i * O_i) given (k_attn_delta), the stored bf16 P of the
-// forward, and dS^T written to global memory for dQ = dS K (a batched GEMM that
-// reads it as an MN-major operand).  dK_j and dV_j go to dQKV in bf16.
+// forward, and dS written to global memory for dQ = dS K (a batched GEMM).  dK_j
+// and dV_j go to dQKV in bf16.
 // Every operand tile is loaded once, as 64-column swizzle atoms of 128 rows: such
 // an atom is also two stacked MN-major chunks of 64 rows, so the same bytes serve
-// as a K-major operand (dP^T, dK's A) and as an MN-major one (dV's A and B, dK's B).
-// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-5 one key row per thread.
-// TMEM: dV at columns 0.., dK at 192.., dP^T at 384 .. 511.
+// as a K-major operand (dO and V for dP) and as an MN-major one (P and dO for dV,
+// dS and Q for dK).
+// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-5 one query row per thread.
+// TMEM: dV at columns 0.., dK at 192.., dP at 384 .. 511.
 // ---------------------------------------------------------------------------
 constexpr int kFbThreads = 64 + 32 * 4;
 constexpr size_t kFbSmemBytes = (size_t)kFaTileBytes * 3 /* V, dO, Q */ + 2 * kFaPBytes /* P, dS^T */ +
@@ -510,7 +511,7 @@ static_assert(kFbSmemBytes <= 232448, "smem budget");
 struct FbParams {
   int L, nh, ns, d, d_pad, n_atoms;
   float alpha;     // 1 / sqrt(d)
-  uint16_t* dST;   // [ns, nh, L keys, L queries] bf16: dS transposed
+  uint16_t* dS;    // [ns, nh, L queries, L keys] bf16
 };
 
 __global__ void __launch_bounds__(kFbThreads, 1)
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kFbThreads, 1)
   uint8_t* sdO = sV + kFaTileBytes;
   uint8_t* sQ = sdO + kFaTileBytes;
   uint8_t* sP = sQ + kFaTileBytes;
-  uint8_t* sDS = sP + kFaPBytes;
+  uint8_t* sDS = sP + kFaPBytes;                   // the dS tile, laid out like P
   float* sDelta = reinterpret_cast<float*>(sDS + kFaPBytes);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sDelta + kFaTile);
   uint64_t* v_full = bar + 0;
@@ -642,18 +643,18 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       // ------------------------------------------------------------ MMA issuer
       constexpr uint32_t idesc_dp = make_idesc_bf16(kFaTile, kFaTile, false, false);
       const uint32_t idesc_dv = make_idesc_bf16(kFaTile, fp.d_pad, true, true);
-      const uint32_t idesc_dk = make_idesc_bf16(kFaTile, fp.d_pad, false, true);
+      const uint32_t idesc_dk = make_idesc_bf16(kFaTile, fp.d_pad, true, true);
       const int nk_d = fp.d_pad / 16;
       const uint32_t t_dv = tmem_base, t_dk = tmem_base + 192u, t_dp = tmem_base + 384u;
       uint32_t nv = 0, ndo = 0, np = 0, nq = 0, ndp = 0, nds = 0, n_item = 0;
       bool ok = true;
-      auto issue_dp = [&]() -> bool {  // dP^T = V dO^T
+      auto issue_dp = [&]() -> bool {  // dP = dO V^T (a query row per TMEM lane)
         if (!mbar_wait(do_full, ndo & 1) || !mbar_wait(dp_empty, (ndp & 1) ^ 1)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(sV), ob = smem_u32(sdO);
         for (int kk = 0; kk < nk_d; ++kk) {
           const uint32_t off = (uint32_t)(kk >> 2) * kFaAtomBytes + (uint32_t)(kk & 3) * 32;
-          umma_bf16(t_dp, make_sdesc_sw128(vb + off, 16, 1024), make_sdesc_sw128(ob + off, 16, 1024), idesc_dp,
+          umma_bf16(t_dp, make_sdesc_sw128(ob + off, 16, 1024), make_sdesc_sw128(vb + off, 16, 1024), idesc_dp,
                     kk > 0 ? 1u : 0u);
         }
         umma_commit(dp_full);
@@ -673,15 +674,13 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         ++np;
         return true;
       };
-      auto issue_dk = [&](bool first) -> bool {  // dK += dS^T Q
+      auto issue_dk = [&](bool first) -> bool {  // dK += dS^T Q (dS^T read as an MN-major operand)
         if (!mbar_wait(ds_full, nds & 1) || !mbar_wait(q_full, nq & 1)) return false;
         tc_fence_after();
         const uint32_t sb_ = smem_u32(sDS), qb = smem_u32(sQ);
-        for (int kk = 0; kk < kFaTile / 16; ++kk) {
-          const uint32_t off = (uint32_t)(kk >> 2) * kFaAtomBytes + (uint32_t)(kk & 3) * 32;
-          umma_bf16(t_dk, make_sdesc_sw128(sb_ + off, 16, 1024), make_sdesc_sw128(qb + kk * 2048, kFaAtomBytes, 1024),
-                    idesc_dk, (first && kk == 0) ? 0u : 1u);
-        }
+        for (int kk = 0; kk < kFaTile / 16; ++kk)
+          umma_bf16(t_dk, make_sdesc_sw128(sb_ + kk * 2048, kFaAtomBytes, 1024),
+                    make_sdesc_sw128(qb + kk * 2048, kFaAtomBytes, 1024), idesc_dk, (first && kk == 0) ? 0u : 1u);
         umma_commit(q_empty);
         umma_commit(ds_empty);
         ++nq;
@@ -707,9 +706,9 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       if (!ok) record_status(status, kStatusTimeout, 32);
     }
   } else {
-    // -------------------------------------------------------------- one key row per thread
+    // -------------------------------------------------------------- one query row per thread
     const int quarter = warp & 3;
-    const int k_in = quarter * 32 + lane;                 // key row within the tile
+    const int q_in = quarter * 32 + lane;                 // query row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     uint32_t np = 0, ndp = 0, nds = 0, n_out = 0, n_item = 0;
     bool ok = true;
@@ -717,7 +716,7 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       int kt, hb, sb;
       decode(item, kt, hb, sb);
       for (int i = kt; i < n_t && ok; ++i) {
-        // dP^T row of key k_in, queries 0 .. 127 of tile i
+        // dP row of query q_in of tile i, keys 0 .. 127 of tile kt
         if (!(ok = mbar_wait(dp_full, ndp & 1))) break;
         tc_fence_after();
         uint32_t dp[128];
@@ -728,42 +727,35 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(dp_empty);
         ++ndp;
-        // P (and delta) of tile (i, kt); the dS^T buffer free: dK's product read it,
+        // P (and delta) of tile (i, kt); the dS buffer free: dK's product read it,
         // and this warp's store of it has read it
         if (!(ok = mbar_wait(p_full, np & 1))) break;
         if (!(ok = mbar_wait(ds_empty, (nds & 1) ^ 1))) break;
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        // P[q][k_in] sits in row q of atom k_in / 64, 16-byte chunk ((k_in % 64) / 8) ^ (q % 8)
-        const uint8_t* pcol = sP + (k_in >> 6) * kFaAtomBytes + (k_in & 7) * 2;
-        const int pchunk = (k_in & 63) >> 3;
-        uint8_t* dsrow = sDS + k_in * 128;
+        const float dl = sDelta[q_in];
+        const uint8_t* prow = sP + q_in * 128;
+        uint8_t* dsrow = sDS + q_in * 128;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {          // queries 8 g .. 8 g + 7
+        for (int g = 0; g < 16; ++g) {          // keys 8 g .. 8 g + 7: atom g / 8, chunk (g % 8) ^ (q_in % 8)
+          const uint32_t off = (g >> 3) * kFaAtomBytes + (((g & 7) ^ (q_in & 7)) << 4);
+          const uint4 pv = *reinterpret_cast<const uint4*>(prow + off);
+          const float pf[8] = {bf16lo(pv.x), bf16hi(pv.x), bf16lo(pv.y), bf16hi(pv.y),
+                               bf16lo(pv.z), bf16hi(pv.z), bf16lo(pv.w), bf16hi(pv.w)};
           uint32_t pk[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float v2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int q = 8 * g + 2 * e + u;
-              const uint16_t pbits = *reinterpret_cast<const uint16_t*>(pcol + q * 128 + ((pchunk ^ (q & 7)) << 4));
-              const float p = __uint_as_float((uint32_t)pbits << 16);
-              v2[u] = p * (__uint_as_float(dp[q]) - sDelta[q]) * fp.alpha;
-            }
-            pk[e] = pack_bf16x2(v2[0], v2[1]);
-          }
-          // dS^T row k_in, queries 8 g ..: atom g / 8, chunk (g % 8) ^ (k_in % 8)
-          *reinterpret_cast<uint4*>(dsrow + (g >> 3) * kFaAtomBytes + (((g & 7) ^ (k_in & 7)) << 4)) =
-              make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int e = 0; e < 4; ++e)
+            pk[e] = pack_bf16x2(pf[2 * e] * (__uint_as_float(dp[8 * g + 2 * e]) - dl) * fp.alpha,
+                                pf[2 * e + 1] * (__uint_as_float(dp[8 * g + 2 * e + 1]) - dl) * fp.alpha);
+          *reinterpret_cast<uint4*>(dsrow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(p_empty);
           for (int a = 0; a < 2; ++a)
-            tma_store_4d(&mDS, sDS + a * kFaAtomBytes + quarter * 32 * 128, i * kFaTile + 64 * a,
-                         kt * kFaTile + quarter * 32, hb, sb);
+            tma_store_4d(&mDS, sDS + a * kFaAtomBytes + quarter * 32 * 128, kt * kFaTile + 64 * a,
+                         i * kFaTile + quarter * 32, hb, sb);
           bulk_commit();
           mbar_arrive(ds_full);
         }
@@ -771,20 +763,21 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         ++nds;
       }
       if (!ok) break;
-      // dS^T tile (key tile kt, query tile kt - 1) lies above the diagonal; the dQ
+      // dS tile (query tile kt - 1, key tile kt) lies above the diagonal; the dQ
       // product of the 256-query tile that holds query tile kt - 1 reads it when kt
       // is odd, so it must hold zeros
       if (kt & 1) {
         for (int rr = 0; rr < 32; rr += 2) {
-          const int key = kt * kFaTile + quarter * 32 + rr + (lane >> 4);
-          if (key < fp.L) {
-            uint16_t* row = fp.dST + (((int64_t)sb * fp.nh + hb) * fp.L + key) * (int64_t)fp.L + (kt - 1) * kFaTile;
-            *reinterpret_cast<uint4*>(row + (lane & 15) * 8) = make_uint4(0, 0, 0, 0);
+          const int q = (kt - 1) * kFaTile + quarter * 32 + rr + (lane >> 4);
+          const int c = kt * kFaTile + (lane & 15) * 8;
+          if (c < fp.L) {
+            uint16_t* row = fp.dS + (((int64_t)sb * fp.nh + hb) * fp.L + q) * (int64_t)fp.L;
+            *reinterpret_cast<uint4*>(row + c) = make_uint4(0, 0, 0, 0);
           }
         }
       }
       // dV and dK: bf16 through 32 x 32 boxes staged in this warp's own rows of the
-      // dS^T buffer (its last store and dK's last product have read them)
+      // dS buffer (its last store and dK's last product have read them)
       if (!(ok = mbar_wait(acc_full, n_item & 1))) break;
       tc_fence_after();
       if (lane == 0) bulk_wait_read<0>();
@@ -822,7 +815,7 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        bulk_wait_read<0>();   // the staged boxes have been read before the next dS^T rows land there
+        bulk_wait_read<0>();   // the staged boxes have been read before the next dS rows land there
         mbar_arrive(acc_empty);
       }
     }

@@ -545,10 +545,10 @@ int attn_core_fused(DeviceState* st, const uint16_t* QKV, uint16_t* P, uint16_t*
   return launch_check(e, "fused attention core");
 }
 
-// The fused attention core of the backward: dK and dV into dQKV, dS^T into dST
-// (P's shape, keys x queries); delta = rowsum(dO * O) must be in `delta`.
+// The fused attention core of the backward: dK and dV into dQKV, dS (P's shape)
+// into dS; delta = rowsum(dO * O) must be in `delta`.
 int attn_core_bwd_fused(DeviceState* st, const uint16_t* QKV, const uint16_t* P, const uint16_t* dO,
-                        const float* delta, uint16_t* dST, uint16_t* dQKV, int h, int nh, int L, int ns,
+                        const float* delta, uint16_t* dS, uint16_t* dQKV, int h, int nh, int L, int ns,
                         cudaStream_t s) {
   const int d = h / nh;
   const int64_t h3 = 3 * (int64_t)h, LL = (int64_t)L * L;
@@ -560,7 +560,7 @@ int attn_core_bwd_fused(DeviceState* st, const uint16_t* QKV, const uint16_t* P,
   fb.d_pad = (d + 15) & ~15;
   fb.n_atoms = (fb.d_pad + 63) / 64;
   fb.alpha = 1.0f / std::sqrt((float)d);
-  fb.dST = dST;
+  fb.dS = dS;
   CUtensorMap mV, mQ, mdO, mP, mDelta, mDS, mdK, mdV;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw128 = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -570,7 +570,7 @@ int attn_core_bwd_fused(DeviceState* st, const uint16_t* QKV, const uint16_t* P,
   if (!rc) rc = make_map4(&mdO, bf, 2, dO, d, L, h, nh, d, ns, (int64_t)L * h, 64, kFaTile, sw128, l2);
   if (!rc) rc = make_map4(&mP, bf, 2, P, L, L, L, nh, LL, ns, nh * LL, 64, kFaTile, sw128, l2);
   if (!rc)
-    rc = make_map4(&mDS, bf, 2, dST, L, L, L, nh, LL, ns, nh * LL, 64, 32, sw128, CU_TENSOR_MAP_L2_PROMOTION_NONE);
+    rc = make_map4(&mDS, bf, 2, dS, L, L, L, nh, LL, ns, nh * LL, 64, 32, sw128, CU_TENSOR_MAP_L2_PROMOTION_NONE);
   if (!rc)
     rc = make_map4(&mdK, bf, 2, dQKV + h, d, L, h3, nh, d, ns, L * h3, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_NONE);
@@ -764,8 +764,8 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
   EpiParams est{};
   est.kind = kEpiStore;
   if (g_attn_fused.load(std::memory_order_relaxed) && ((d + 15) & ~15) <= kFaMaxAtoms * 64) {
-    // delta = rowsum(dO * O); then, fused per (sequence, head, key tile): dV and dK,
-    // and dS^T for dQ = dS K (a batched GEMM reading dS^T as an MN-major operand)
+    // delta = rowsum(dO * O); then, fused per (sequence, head, key tile): dV, dK and
+    // dS, and dQ = dS K as a batched GEMM
     float* delta = dP;
     {
       const int64_t warps = tokens * nh;
@@ -780,7 +780,7 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
     }
     rc = attn_core_bwd_fused(st, QKV, P, dO, delta, dS, dQKV, h, nh, L, ns, s);
     if (rc) return rc;
-    rc = gemm_batched(st, {dS, true, L, L, L, LL, nh * LL}, {QKV + h, true, d, L, h3, d, L * h3},
+    rc = gemm_batched(st, {dS, false, L, L, L, LL, nh * LL}, {QKV + h, true, d, L, h3, d, L * h3},
                       {dQKV, d, L, h3, d, L * h3}, L, d, L, nh, ns, est, s, kTraceAttnGemm, kCausalKUpTo);
     if (rc) return rc;
   } else {
