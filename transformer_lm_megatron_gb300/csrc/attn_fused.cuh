@@ -500,10 +500,12 @@ namespace gbmlp {
 // an atom is also two stacked MN-major chunks of 64 rows, so the same bytes serve
 // as a K-major operand (dO and V for dP) and as an MN-major one (P and dO for dV,
 // dS and Q for dK).
-// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-5 one query row per thread.
+// Warps: 0 TMA producer, 1 TMEM owner and MMA issuer, 2-9 one query row per thread,
+// two warps per row (TMEM lane quarter), each on half of the 128 keys of a tile.
 // TMEM: dV at columns 0.., dK at 192.., dP at 384 .. 511.
 // ---------------------------------------------------------------------------
-constexpr int kFbThreads = 64 + 32 * 4;
+constexpr int kFbRowWarps = 8;          // two per TMEM lane quarter, each on 64 of a tile's 128 keys
+constexpr int kFbThreads = 64 + 32 * kFbRowWarps;
 constexpr size_t kFbSmemBytes = (size_t)kFaTileBytes * 3 /* V, dO, Q */ + 2 * kFaPBytes /* P, dS^T */ +
                                 kFaTile * sizeof(float) /* delta */ + 1024 /*align*/ + 256 /*barriers*/;
 static_assert(kFbSmemBytes <= 232448, "smem budget");
@@ -561,13 +563,13 @@ __global__ void __launch_bounds__(kFbThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     mbar_init(p_full, 1);
-    mbar_init(p_empty, 1 + 4);   // the products that read P, and the 4 warps that read it
+    mbar_init(p_empty, 1 + kFbRowWarps);   // the products that read P, and the warps that read it
     mbar_init(dp_full, 1);
-    mbar_init(dp_empty, 4);
-    mbar_init(ds_full, 4);
+    mbar_init(dp_empty, kFbRowWarps);
+    mbar_init(ds_full, kFbRowWarps);
     mbar_init(ds_empty, 1);
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, kFbRowWarps);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -708,6 +710,7 @@ __global__ void __launch_bounds__(kFbThreads, 1)
   } else {
     // -------------------------------------------------------------- one query row per thread
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;                     // keys 64 half .. 64 half + 63 of each tile
     const int q_in = quarter * 32 + lane;                 // query row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
     uint32_t np = 0, ndp = 0, nds = 0, n_out = 0, n_item = 0;
@@ -719,9 +722,10 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         // dP row of query q_in of tile i, keys 0 .. 127 of tile kt
         if (!(ok = mbar_wait(dp_full, ndp & 1))) break;
         tc_fence_after();
-        uint32_t dp[128];
+        uint32_t dp[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(t_lane + 384u + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&dp[32 * c]));
+        for (int c = 0; c < 2; ++c)
+          tmem_ld_32x32b_x32(t_lane + 384u + 64u * half + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&dp[32 * c]));
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
@@ -734,11 +738,11 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
         const float dl = sDelta[q_in];
-        const uint8_t* prow = sP + q_in * 128;
-        uint8_t* dsrow = sDS + q_in * 128;
+        const uint8_t* prow = sP + half * kFaAtomBytes + q_in * 128;
+        uint8_t* dsrow = sDS + half * kFaAtomBytes + q_in * 128;
 #pragma unroll
-        for (int g = 0; g < 16; ++g) {          // keys 8 g .. 8 g + 7: atom g / 8, chunk (g % 8) ^ (q_in % 8)
-          const uint32_t off = (g >> 3) * kFaAtomBytes + (((g & 7) ^ (q_in & 7)) << 4);
+        for (int g = 0; g < 8; ++g) {           // keys 64 half + 8 g ..: chunk g ^ (q_in % 8) of atom `half`
+          const uint32_t off = (uint32_t)((g ^ (q_in & 7)) << 4);
           const uint4 pv = *reinterpret_cast<const uint4*>(prow + off);
           const float pf[8] = {bf16lo(pv.x), bf16hi(pv.x), bf16lo(pv.y), bf16hi(pv.y),
                                bf16lo(pv.z), bf16hi(pv.z), bf16lo(pv.w), bf16hi(pv.w)};
@@ -753,9 +757,8 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(p_empty);
-          for (int a = 0; a < 2; ++a)
-            tma_store_4d(&mDS, sDS + a * kFaAtomBytes + quarter * 32 * 128, kt * kFaTile + 64 * a,
-                         i * kFaTile + quarter * 32, hb, sb);
+          tma_store_4d(&mDS, sDS + half * kFaAtomBytes + quarter * 32 * 128, kt * kFaTile + 64 * half,
+                       i * kFaTile + quarter * 32, hb, sb);
           bulk_commit();
           mbar_arrive(ds_full);
         }
@@ -767,8 +770,8 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       // product of the 256-query tile that holds query tile kt - 1 reads it when kt
       // is odd, so it must hold zeros
       if (kt & 1) {
-        for (int rr = 0; rr < 32; rr += 2) {
-          const int q = (kt - 1) * kFaTile + quarter * 32 + rr + (lane >> 4);
+        for (int rr = half; rr < 32; rr += 4) {
+          const int q = (kt - 1) * kFaTile + quarter * 32 + rr + 2 * (lane >> 4);
           const int c = kt * kFaTile + (lane & 15) * 8;
           if (c < fp.L) {
             uint16_t* row = fp.dS + (((int64_t)sb * fp.nh + hb) * fp.L + q) * (int64_t)fp.L;
@@ -782,11 +785,11 @@ __global__ void __launch_bounds__(kFbThreads, 1)
       tc_fence_after();
       if (lane == 0) bulk_wait_read<0>();
       __syncwarp();
-      uint8_t* my_o = sDS + quarter * 32 * 128;   // 4 KB: two boxes
+      uint8_t* my_o = sDS + half * kFaAtomBytes + quarter * 32 * 128;   // 4 KB: two boxes
       for (int which = 0; which < 2; ++which) {
         const uint32_t col0 = which == 0 ? 0u : 192u;
         const CUtensorMap* map = which == 0 ? &mdV : &mdK;
-        for (int c0 = 0; c0 < fp.d_pad; c0 += 32) {
+        for (int c0 = 32 * half; c0 < fp.d_pad; c0 += 64) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(t_lane + col0 + (uint32_t)c0, r);
           tmem_ld_wait();
