@@ -25,9 +25,9 @@
 //              buffers; in pass 2 S_{j+1} is issued before O += P_j V_j so the
 //              softmax of one tile overlaps the products of the next.
 //   warps 2-9  one query row per thread (TMEM lane quarter warp % 4), two warps
-//              per row: each takes every other key tile for the softmax and the
-//              bf16 P tile, then half of the zeros above the diagonal and half of
-//              the bf16 O columns.
+//              per row, each on 64 of the 128 keys of every tile (their row
+//              statistics merged once per item), then half of the zeros above the
+//              diagonal and half of the bf16 O columns.
 // Every wait is bounded; on timeout the kernel records kStatusTimeout in the
 // status word and stops.
 #pragma once
@@ -52,9 +52,9 @@ constexpr uint32_t kFaTmemCols = 512;                // S buffers at 0 and 128, 
 // Q, the K/V ring, two P buffers (which also stage the O stores at the end of an
 // item), barriers, and the softmax halves' partial maxima and sums.
 constexpr size_t kFaSmemBytes = (size_t)kFaTileBytes * (1 + kFaStages) + 2 * kFaPBytes + 1024 /*align*/ +
-                                256 /*barriers*/ + 2 * 128 * 2 * sizeof(float);
+                                256 /*barriers*/ + 2 * 2 * 128 * 2 * sizeof(float);
 static_assert(kFaSmemBytes <= 232448, "smem budget");
-static_assert(kFaSoftmaxWarps * 2 * kFaOStageBytes <= 2 * kFaPBytes, "O staging fits in the P buffers");
+static_assert(2 * kFaOStageBytes <= 32 * 128, "O staging fits in a warp's rows of a P buffer");
 constexpr float kLog2e = 1.4426950408889634f;      // log2(e): exp(x) = 2^(x log2 e)
 
 // 2^x with the hardware approximation (ex2.approx, flush-to-zero); 2^-inf = 0.
@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&s_empty[b], kFaSoftmaxWarps / 2);   // the 4 warps of the half that read it
-      mbar_init(&p_full[b], kFaSoftmaxWarps / 2);
+      mbar_init(&s_empty[b], kFaSoftmaxWarps);   // every softmax warp reads its half of each S tile
+      mbar_init(&p_full[b], kFaSoftmaxWarps);
       mbar_init(&p_empty[b], 1);
     }
     mbar_init(o_full, 1);
@@ -300,15 +300,15 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
   } else {
     // -------------------------------------------------------------- softmax / epilogue
-    // Two warps per TMEM lane quarter: the warp of half h takes the key tiles j
-    // with j % 2 == h.  Pass 1 gives each half a partial maximum and sum per row,
-    // merged through shared memory; pass 2 writes the P tiles of its key tiles;
-    // the O columns are shared out by 32-column block.
+    // Two warps per TMEM lane quarter: the warp of half h takes keys 64 h .. 64 h + 63
+    // of every key tile.  Pass 1 gives each half a partial maximum and sum per row,
+    // merged through shared memory; pass 2 writes its half of every P tile; the O
+    // columns are shared out by 32-column block.
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r_in = quarter * 32 + lane;                  // query row within the tile
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    float* s_ml = reinterpret_cast<float*>(tmem_slot + 4);  // [2 halves][128 rows][m, l]
+    float* s_ml = reinterpret_cast<float*>(tmem_slot + 4);  // [2 items][2 halves][128 rows][m, l]
     const float al = fp.alpha * kLog2e;                     // scores in units of log2
     uint32_t sc = 0, pc = 0, n_out = 0;
     bool ok = true;
@@ -317,102 +317,93 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       int qt, hb, sb;
       decode(item, qt, hb, sb);
       const int nkv = qt + 1;
-      // pass 1: this half's running maximum (log2 units) and sum of the row
+      // pass 1: the running maximum (log2 units) and sum of the row over this half's
+      // 64 keys of every key tile
       float m = -INFINITY, l = 0.0f;
       for (int j = 0; j < nkv && ok; ++j, ++sc) {
-        if ((j & 1) != half) continue;
         const int b = (int)(sc & 1);
         if (!(ok = mbar_wait(&s_full[b], (sc >> 1) & 1))) break;
         tc_fence_after();
-        const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile);
+        const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile + 64 * half);
         const bool diag = j == qt;
-        // 32-column blocks, the next block's TMEM load in flight while this one is processed
-        uint32_t ra[32], rb[32];
-        tmem_ld_32x32b_x32(t_s, ra);
+        uint32_t r[2][32];
+        tmem_ld_32x32b_x32(t_s, r[0]);
+        tmem_ld_32x32b_x32(t_s + 32, r[1]);
         tmem_ld_wait();
-#pragma unroll
-        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
-          uint32_t (&r)[32] = (c0 & 32) ? rb : ra;
-          if (c0 + 32 < kFaTile) tmem_ld_32x32b_x32(t_s + c0 + 32, (c0 & 32) ? ra : rb);
-          float mx = -INFINITY;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float v = (diag && c0 + k > r_in) ? -INFINITY : al * __uint_as_float(r[k]);
-            r[k] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
-          const float m_new = fmaxf(m, mx);
-          float sum = 0.0f;
-#pragma unroll
-          for (int k = 0; k < 32; ++k) sum += ex2_approx(__uint_as_float(r[k]) - m_new);
-          l = (m == -INFINITY ? 0.0f : l * ex2_approx(m - m_new)) + sum;
-          m = m_new;
-          tmem_ld_wait();
-        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&s_empty[b]);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int c0 = 64 * half + 32 * c;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const float v = (diag && c0 + k > r_in) ? -INFINITY : al * __uint_as_float(r[c][k]);
+            r[c][k] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+          const float m_new = fmaxf(m, mx);
+          const float m_ref = m_new == -INFINITY ? 0.0f : m_new;   // a block with every key masked adds 0
+          float sum = 0.0f;
+#pragma unroll
+          for (int k = 0; k < 32; ++k) sum += ex2_approx(__uint_as_float(r[c][k]) - m_ref);
+          l = (m == -INFINITY ? 0.0f : l * ex2_approx(m - m_new)) + sum;
+          m = m_new;
+        }
       }
       if (!ok) break;
-      // merge the two halves (the same expression, in the same order, in both);
-      // the barrier also orders this item's P writes after every warp's O stores
-      // of the previous item have read the shared memory they reuse
-      if (lane == 0) bulk_wait_read<0>();
-      s_ml[(half * 128 + r_in) * 2] = m;
-      s_ml[(half * 128 + r_in) * 2 + 1] = l;
+      // merge the two halves (the same expression, in the same order, in both),
+      // through one of two buffers by item parity
+      float* ml = s_ml + (n_item & 1) * (2 * 128 * 2);
+      ml[(half * 128 + r_in) * 2] = m;
+      ml[(half * 128 + r_in) * 2 + 1] = l;
       fa_softmax_sync();
-      const float m0 = s_ml[r_in * 2], l0 = s_ml[r_in * 2 + 1];
-      const float m1 = s_ml[(128 + r_in) * 2], l1 = s_ml[(128 + r_in) * 2 + 1];
+      const float m0 = ml[r_in * 2], l0 = ml[r_in * 2 + 1];
+      const float m1 = ml[(128 + r_in) * 2], l1 = ml[(128 + r_in) * 2 + 1];
       m = fmaxf(m0, m1);
       l = (m0 == -INFINITY ? 0.0f : l0 * ex2_approx(m0 - m)) + (m1 == -INFINITY ? 0.0f : l1 * ex2_approx(m1 - m));
       const float inv = 1.0f / l;
-      // pass 2: P_j = exp(S_j - max) / sum to shared memory (operand of O += P V) and to P
+      // pass 2: this half's 64 columns of P_j = exp(S_j - max) / sum, to shared memory
+      // (operand of O += P V) and to P
       for (int j = 0; j < nkv && ok; ++j, ++sc, ++pc) {
-        if ((j & 1) != half) continue;
         const int b = (int)(sc & 1);
         const int pb = (int)(pc & 1);
         if (!(ok = mbar_wait(&s_full[b], (sc >> 1) & 1))) break;
         tc_fence_after();
-        // the P buffer is free once the products that read it are done and this
-        // warp's store of its rows two tiles ago has read it
+        const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile + 64 * half);
+        uint32_t r[2][32];
+        tmem_ld_32x32b_x32(t_s, r[0]);
+        tmem_ld_32x32b_x32(t_s + 32, r[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_empty[b]);
+        // this warp's rows of the P buffer are free once the products that read it
+        // are done and this warp's store of them (or of O) has read them
         if (!(ok = mbar_wait(&p_empty[pb], ((pc >> 1) & 1) ^ 1))) break;
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
-        const uint32_t t_s = t_lane + (uint32_t)(b * kFaTile);
-        uint8_t* pbuf = sP + pb * kFaPBytes;
+        uint8_t* atom = sP + pb * kFaPBytes + half * kFaAtomBytes;
+        uint8_t* row = atom + r_in * 128;
         const bool diag = j == qt;
-        uint32_t ra[32], rb[32];
-        tmem_ld_32x32b_x32(t_s, ra);
-        tmem_ld_wait();
 #pragma unroll
-        for (int c0 = 0; c0 < kFaTile; c0 += 32) {
-          uint32_t (&r)[32] = (c0 & 32) ? rb : ra;
-          if (c0 + 32 < kFaTile) tmem_ld_32x32b_x32(t_s + c0 + 32, (c0 & 32) ? ra : rb);
-          // row r_in, keys c0 .. c0 + 31: 4 chunks of 8 keys in the 128-byte swizzle of atom c0 / 64
-          uint8_t* atom = pbuf + (c0 >> 6) * kFaAtomBytes + r_in * 128;
+        for (int g = 0; g < 8; ++g) {         // keys 64 half + 8 g .. + 7: chunk g ^ (r_in % 8) of the atom
+          uint32_t pk[4];
 #pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint32_t pk[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int k0 = 8 * g + 2 * k, k1 = k0 + 1;
-              const float p0 = (diag && c0 + k0 > r_in) ? 0.0f : ex2_approx(fmaf(__uint_as_float(r[k0]), al, -m)) * inv;
-              const float p1 = (diag && c0 + k1 > r_in) ? 0.0f : ex2_approx(fmaf(__uint_as_float(r[k1]), al, -m)) * inv;
-              pk[k] = pack_bf16x2(p0, p1);
-            }
-            const int chunk = ((c0 & 63) >> 3) + g;
-            *reinterpret_cast<uint4*>(atom + ((chunk ^ (r_in & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          for (int k = 0; k < 4; ++k) {
+            const int k0 = 8 * g + 2 * k, k1 = k0 + 1;    // 0 .. 63 within the half
+            const float s0 = __uint_as_float(r[k0 >> 5][k0 & 31]), s1 = __uint_as_float(r[k1 >> 5][k1 & 31]);
+            const float p0 = (diag && 64 * half + k0 > r_in) ? 0.0f : ex2_approx(fmaf(s0, al, -m)) * inv;
+            const float p1 = (diag && 64 * half + k1 > r_in) ? 0.0f : ex2_approx(fmaf(s1, al, -m)) * inv;
+            pk[k] = pack_bf16x2(p0, p1);
           }
-          tmem_ld_wait();
+          *reinterpret_cast<uint4*>(row + ((g ^ (r_in & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         }
-        tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&s_empty[b]);
-          for (int a = 0; a < 2; ++a)
-            tma_store_4d(&mP, pbuf + a * kFaAtomBytes + quarter * 32 * 128, j * kFaTile + 64 * a,
-                         qt * kFaTile + quarter * 32, hb, sb);
+          tma_store_4d(&mP, atom + quarter * 32 * 128, j * kFaTile + 64 * half, qt * kFaTile + quarter * 32, hb, sb);
           bulk_commit();
           mbar_arrive(&p_full[pb]);
         }
@@ -427,19 +418,19 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           for (int rr = half; rr < 32; rr += 2) {
             const int qq = qt * kFaTile + quarter * 32 + rr;
             if (qq >= fp.L) break;
-            uint16_t* row = fp.P + (((int64_t)sb * fp.nh + hb) * fp.L + qq) * (int64_t)fp.L + c_begin;
-            for (int c = lane * 8; c < z; c += 256) *reinterpret_cast<uint4*>(row + c) = make_uint4(0, 0, 0, 0);
+            uint16_t* prow = fp.P + (((int64_t)sb * fp.nh + hb) * fp.L + qq) * (int64_t)fp.L + c_begin;
+            for (int c = lane * 8; c < z; c += 256) *reinterpret_cast<uint4*>(prow + c) = make_uint4(0, 0, 0, 0);
           }
         }
       }
-      // every warp's P stores have read the P buffers, which now stage O
+      // this warp's P stores have read its rows of the first P buffer, which now stage O
       if (lane == 0) bulk_wait_read<0>();
-      fa_softmax_sync();
+      __syncwarp();
       if (!(ok = mbar_wait(o_full, n_item & 1))) break;
       tc_fence_after();
       // O: the accumulator is final; bf16 through 32 x 32 boxes, the column blocks
-      // shared out between the halves, staged in the P buffers
-      uint8_t* my_o = sP + (warp - 2) * 2 * kFaOStageBytes;
+      // shared out between the halves, staged in this warp's rows of the first P buffer
+      uint8_t* my_o = sP + half * kFaAtomBytes + quarter * 32 * 128;
       for (int c0 = 32 * half; c0 < fp.d_pad; c0 += 64) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(t_lane + 256u + (uint32_t)c0, r);
