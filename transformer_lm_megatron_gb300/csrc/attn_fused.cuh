@@ -606,6 +606,15 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         mbar_arrive_expect_tx(v_full, tile_tx);
         for (int a = 0; a < fp.n_atoms; ++a) tma_load_4d(sV + a * kFaAtomBytes, &mV, v_full, 64 * a, kt * kFaTile, hb, sb);
         ++nv;
+        // in the order the MMA issuer frees them: dO_i and P_i, then Q_{i-1} (the
+        // product dK += dS^T Q of a tile comes after dP and dV of the next one)
+        auto load_q = [&](int i) -> bool {
+          if (!mbar_wait(q_empty, (nq & 1) ^ 1)) return false;
+          mbar_arrive_expect_tx(q_full, tile_tx);
+          for (int a = 0; a < fp.n_atoms; ++a) tma_load_4d(sQ + a * kFaAtomBytes, &mQ, q_full, 64 * a, i * kFaTile, hb, sb);
+          ++nq;
+          return true;
+        };
         for (int i = kt; i < n_t && ok; ++i) {
           if (!(ok = mbar_wait(do_empty, (ndo & 1) ^ 1))) break;
           mbar_arrive_expect_tx(do_full, tile_tx);
@@ -618,11 +627,9 @@ __global__ void __launch_bounds__(kFbThreads, 1)
             tma_load_4d(sP + a * kFaAtomBytes, &mP, p_full, kt * kFaTile + 64 * a, i * kFaTile, hb, sb);
           tma_load_2d(sDelta, &mDelta, p_full, i * kFaTile, sb * fp.nh + hb, 0, false);
           ++np;
-          if (!(ok = mbar_wait(q_empty, (nq & 1) ^ 1))) break;
-          mbar_arrive_expect_tx(q_full, tile_tx);
-          for (int a = 0; a < fp.n_atoms; ++a) tma_load_4d(sQ + a * kFaAtomBytes, &mQ, q_full, 64 * a, i * kFaTile, hb, sb);
-          ++nq;
+          if (i > kt) ok = load_q(i - 1);
         }
+        if (ok) ok = load_q(n_t - 1);
       }
       if (!ok) record_status(status, kStatusTimeout, 30);
       // drain: every copy issued has landed before the CTA may exit
@@ -688,8 +695,10 @@ __global__ void __launch_bounds__(kFbThreads, 1)
         // the previous item's dK and dV have been read out of tensor memory
         if (!(ok = mbar_wait(acc_empty, (n_item & 1) ^ 1))) break;
         tc_fence_after();
+        // dP and dV of query tile i, then dK of tile i - 1 (whose dS the threads have
+        // been computing meanwhile)
         ok = issue_dp() && issue_dv(true);
-        for (int i = kt + 1; i < n_t && ok; ++i) ok = issue_dp() && issue_dk(i - 1 == kt) && issue_dv(false);
+        for (int i = kt + 1; i < n_t && ok; ++i) ok = issue_dp() && issue_dv(false) && issue_dk(i - 1 == kt);
         if (ok) ok = issue_dk(n_t - 1 == kt);
         if (ok) {
           umma_commit(v_empty);
