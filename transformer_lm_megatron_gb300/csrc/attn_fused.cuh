@@ -64,11 +64,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-// Barrier of the softmax warps only (named barrier 1; warps 2 .. 2 + kFaSoftmaxWarps - 1).
-__device__ __forceinline__ void fa_softmax_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(32 * kFaSoftmaxWarps) : "memory");
-}
-
 struct FaParams {
   int L;          // sequence length (keys and queries per sequence)
   int nh;         // heads
@@ -103,7 +98,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   uint64_t* p_empty = p_full + 2;              // [2]
   uint64_t* o_full = p_empty + 2;
   uint64_t* o_empty = o_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_empty + 1);
+  uint64_t* merged = o_empty + 1;              // the softmax warps' row statistics are in shared memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(merged + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -128,6 +124,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     }
     mbar_init(o_full, 1);
     mbar_init(o_empty, kFaSoftmaxWarps);
+    mbar_init(merged, kFaSoftmaxWarps);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -358,7 +355,11 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       float* ml = s_ml + (n_item & 1) * (2 * 128 * 2);
       ml[(half * 128 + r_in) * 2] = m;
       ml[(half * 128 + r_in) * 2 + 1] = l;
-      fa_softmax_sync();
+      // every softmax warp has written its statistics (a bounded wait, like every other:
+      // a warp that gave up earlier never arrives, and the others give up in turn)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merged);
+      if (!(ok = mbar_wait(merged, n_item & 1))) break;
       const float m0 = ml[r_in * 2], l0 = ml[r_in * 2 + 1];
       const float m1 = ml[(128 + r_in) * 2], l1 = ml[(128 + r_in) * 2 + 1];
       m = fmaxf(m0, m1);
