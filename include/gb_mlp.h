@@ -118,7 +118,11 @@ int mlp_fwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
  *   dZ     [tokens, h]  workspace/output: gradient after dropout (bf16).
  *   dU     [tokens, ffn] workspace/output: gradient of the pre-activation (bf16).
  *   dXacc  [tokens, h] fp32 workspace for the sum over slices of one-slice
- *                        calls; may be NULL when t == 1 or slice == -1.
+ *                        calls; may be NULL when t == 1 or slice == -1.  In
+ *                        those calls a non-NULL dXacc serves instead as scratch
+ *                        for transposed bf16 copies of X and dZ that speed up
+ *                        the weight-gradient GEMMs (mlp_set_wgrad_transpose);
+ *                        either way its contents are undefined afterwards.
  *   dX     [tokens, h]  output (overwritten).
  *   dA, da, dB, db    fp32 gradient accumulators (+= or =, see accumulate).
  * Returns MLP_OK or an error code.
@@ -264,6 +268,25 @@ int mlp_set_dependent_launch(int enable);
 int mlp_set_split_tail(int enable);
 
 /*
+ * mlp_set_wgrad_transpose - how mlp_bwd feeds the weight-gradient GEMMs
+ * dB (+)= Y^T dZ and dA (+)= X^T dU, whose reduction runs over the tokens, so
+ * that both operands of each are MN-major as stored (a GEMM with two MN-major
+ * operands runs about 5 % slower than with one K-major operand), for later calls
+ * in this process:
+ *   1  whenever dXacc is free (t == 1 or slice == -1), passed and 16-byte
+ *      aligned, tokens % 8 == 0 and tokens > 960, and both GEMMs run on CTA pairs
+ *      (see mlp_set_cta_pair): one extra launch writes X^T and dZ^T
+ *      ([h, tokens] bf16 each) into dXacc, and the two GEMMs read those copies as
+ *      K-major operands;
+ *  -1  (the default) the same, for GEMMs of at least 1e12 FLOP each (smaller ones
+ *      do not repay the copies);
+ *   0  never.
+ * The products and their reduction order are the same either way.  Returns
+ * MLP_OK or MLP_EINVAL.
+ */
+int mlp_set_wgrad_transpose(int mode);
+
+/*
  * mlp_set_attn_fused - choose, for later attn_fwd / attn_bwd calls in this
  * process, how the attention core runs: 1 (the default) fused kernels when the
  * head size d is at most 192, 0 the unfused launches.
@@ -309,7 +332,8 @@ int mlp_trace_begin(int capacity);
  * mlp_trace_end - stop tracing, wait for the traced launches and report up to
  * max_entries of them in launch order: kinds[i] (0..5 = the GEMMs F1, F2, B2, B3,
  * B4, B5 of the forward/backward; 10 = dropout backward + db; 11 = column sum
- * for da; 12 = accumulator reset; 14 = adam_step; 20 = attention GEMMs; 21 =
+ * for da; 12 = accumulator reset; 14 = adam_step; 15 = the transposed copies of
+ * X and dZ (mlp_set_wgrad_transpose); 20 = attention GEMMs; 21 =
  * softmax forward / backward; 22 = fused attention core), mnk[3i..3i+2] = the
  * launch's M, N, K (GEMMs; for the fused core: query rows, keys per sequence, d)
  * or rows, columns, 0, and ms[i] = its device time in milliseconds.  Any output

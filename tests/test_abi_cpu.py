@@ -118,6 +118,10 @@ def test_switches_reject_bad_values(lib):
     assert lib.mlp_set_tile_scheduler(2) == mlp.MLP_EINVAL
     assert lib.mlp_set_attn_fused(2) == mlp.MLP_EINVAL
     assert lib.mlp_set_attn_fused(1) == mlp.MLP_OK
+    assert lib.mlp_set_wgrad_transpose(2) == mlp.MLP_EINVAL
+    assert lib.mlp_set_wgrad_transpose(-2) == mlp.MLP_EINVAL
+    for mode in (0, 1, -1):
+        assert lib.mlp_set_wgrad_transpose(mode) == mlp.MLP_OK
     assert lib.mlp_set_tile_scheduler(-1) == mlp.MLP_OK
     for fn in (lib.mlp_set_cta_pair, lib.mlp_set_dependent_launch, lib.mlp_set_split_tail, lib.mlp_set_tile_scheduler):
         assert fn(1) == mlp.MLP_OK

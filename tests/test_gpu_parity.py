@@ -406,6 +406,44 @@ def test_tile_scheduler_changes_no_bit(tokens, h, ffn, t, mode, cta_pair_mode, t
     compare_full(s, [o_dy[-1]], g_dy, [r_outs[-1]], r_grads, label="dynamic tile order")
 
 
+@pytest.fixture
+def wgrad_transpose():
+    yield
+    mlp.mlp_set_wgrad_transpose(-1)
+
+
+@pytest.mark.parametrize("tokens,h,ffn,t", [
+    (1024, 256, 1024, 1),     # whole 64 x 64 tiles of the copies
+    (1000, 264, 1056, 1),     # ragged copy tiles along both dimensions
+    (1000, 384, 1536, 4),     # every slice in one call, t = 4
+])
+def test_wgrad_transposed_operands_change_no_bit(tokens, h, ffn, t, wgrad_transpose):
+    """B3 and B4 reading transposed copies of dZ and X (K-major operands held in
+    dXacc) give, bit for bit, what they give reading dZ and X as MN-major
+    operands: the same products, reduced in the same order.  The copy launch runs
+    once per micro-batch when asked for and never otherwise.  Two micro-batches,
+    so the second adds its gradients (reduce-add epilogues) to the first's."""
+    s = Shape(tokens=tokens, h=h, ffn=ffn, t=t, k=2)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    runs = {}
+    for mode in (0, 1):
+        mlp.mlp_set_wgrad_transpose(mode)
+        tr = mlp.Trace(capacity=256)
+        tr.start()
+        runs[mode] = run_gpu(s, w_dev, mbs_dev, slice_mode="all", keep_all=True)
+        tr.stop()
+        copies = sum(1 for kind, _, _ in tr.entries if kind == 15)
+        assert copies == (s.k if mode == 1 else 0), (mode, copies)
+    (o_mn, g_mn), (o_k, g_k) = runs[0], runs[1]
+    for j in range(s.k):
+        for k in o_mn[j]:
+            assert torch.equal(o_k[j][k], o_mn[j][k]), (j, k)
+    for k in g_mn:
+        assert torch.equal(g_k[k], g_mn[k]), k
+    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
+    compare_full(s, [o_k[-1]], g_k, [r_outs[-1]], r_grads, label="transposed weight-gradient operands")
+
+
 @pytest.mark.parametrize("mode", ["all", "each"])
 def test_cuda_graph_replay_equals_eager(mode):
     """A step captured in a CUDA graph and replayed gives, bit for bit, what the

@@ -2,7 +2,8 @@
 //   * dropout backward + bias gradient:  dZ = dO * m / (1-p) (bf16),  db (+)= sum_tok dZ
 //   * column sums:                        da_i (+)= sum_tok dU_i
 //   (+)= adds to the accumulator, or overwrites it for the first micro-batch of a step
-//   * gradient-accumulator reset, the dropout mask itself, and a GeLU probe.
+//   * gradient-accumulator reset, transposed copies of bf16 matrices, the dropout
+//     mask itself, and a GeLU probe.
 //
 // Column sums are deterministic: a cluster of 1 to 8 CTAs (as many as keep the
 // grid resident in one wave) owns 64 columns, each CTA a fixed share of the rows; each of a
@@ -150,6 +151,57 @@ __global__ void k_zero_f32(float* __restrict__ p, int64_t n) {
   float4* p4 = reinterpret_cast<float4*>(p);
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x)
     p4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// Transposed copies: out[c * rows + r] = in[r * cols + c] for one or two bf16
+// matrices of [rows, cols] (blockIdx.z picks the job).  A CTA moves a 64 x 64 tile
+// through shared memory, with 16-byte loads along the input's rows and 16-byte
+// stores along the output's.  rows % 8 == 0 and cols % 8 == 0, so that every
+// vector lies wholly inside or wholly outside the matrix.
+// Grid (ceil(cols / 64), ceil(rows / 64), jobs).
+constexpr int kTrTile = 64;
+constexpr int kTrThreads = 256;
+struct TransposeJob {
+  const uint16_t* in;
+  uint16_t* out;
+};
+__global__ void __launch_bounds__(kTrThreads)
+    k_transpose_bf16(TransposeJob j0, TransposeJob j1, int64_t rows, int cols) {
+  __shared__ uint16_t tile[kTrTile][kTrTile + 2];   // 132-byte rows: conflict-free 2-byte stores
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const TransposeJob j = blockIdx.z == 0 ? j0 : j1;
+  const int64_t r0 = (int64_t)blockIdx.y * kTrTile;
+  const int c0 = blockIdx.x * kTrTile;
+  const int v = threadIdx.x & 7;                    // which 8-element vector of a 64-element segment
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int rr = (threadIdx.x >> 3) + 32 * u;     // input row within the tile
+    const int64_t r = r0 + rr;
+    const int c = c0 + 8 * v;
+    uint4 q = make_uint4(0, 0, 0, 0);
+    if (r < rows && c < cols) q = *reinterpret_cast<const uint4*>(j.in + r * cols + c);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      tile[rr][8 * v + 2 * k] = (uint16_t)(w[k] & 0xffffu);
+      tile[rr][8 * v + 2 * k + 1] = (uint16_t)(w[k] >> 16);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int cc = (threadIdx.x >> 3) + 32 * u;     // output row (input column) within the tile
+    const int c = c0 + cc;
+    const int64_t r = r0 + 8 * v;
+    if (c < cols && r < rows) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        w[k] = (uint32_t)tile[8 * v + 2 * k][cc] | ((uint32_t)tile[8 * v + 2 * k + 1][cc] << 16);
+      *reinterpret_cast<uint4*>(j.out + (int64_t)c * rows + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
 }
 
 // m[r * cols + c] = keep(r, c) ? 1 : 0, eight columns per thread with the same

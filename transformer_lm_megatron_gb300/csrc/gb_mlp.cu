@@ -70,7 +70,7 @@ TraceState g_trace;
 // Kernel identifiers reported by the trace.
 enum TraceKind {
   kTraceF1 = 0, kTraceF2 = 1, kTraceB2 = 2, kTraceB3 = 3, kTraceB4 = 4, kTraceB5 = 5,
-  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13, kTraceAdam = 14,
+  kTraceDropBwd = 10, kTraceColsum = 11, kTraceZero = 12, kTraceOther = 13, kTraceAdam = 14, kTraceTranspose = 15,
   kTraceAttnGemm = 20, kTraceSoftmax = 21, kTraceAttnCore = 22
 };
 
@@ -285,6 +285,27 @@ unsigned dropout_bwd_split(const DeviceState* st, int64_t cols) {
   return split;
 }
 
+// Transposed operands for the weight-gradient GEMMs (mlp_set_wgrad_transpose).
+std::atomic<int> g_wgrad_transpose{-1};
+// Below this size per GEMM the copies cost more than they save (the mid workload's
+// 0.27 TFLOP weight-gradient GEMMs: 6 us saved, 14 us of copies).
+constexpr double kWgradTransposeMinFlop = 1e12;
+
+// Whether mlp_bwd's all-slices call gives B3 and B4 one K-major operand each
+// through transposed copies of dZ and X held in dXacc: the switch allows it, dXacc
+// is there and 16-byte aligned, the token count suits the copies and the tensor
+// maps (a multiple of 8), and both GEMMs take the CTA-pair form with a reduction of
+// 16 k-blocks or more (the forms the (K, MN) and (MN, K) launches instantiate);
+// by default, only GEMMs large enough to repay the copies.
+bool wgrad_transposed(int h, int f, int64_t T, const float* dXacc) {
+  const int mode = g_wgrad_transpose.load(std::memory_order_relaxed);
+  if (mode == 0 || dXacc == nullptr || (reinterpret_cast<uintptr_t>(dXacc) & 15) != 0) return false;
+  if (T % 8 != 0 || (T + kTrTile - 1) / kTrTile > 65535) return false;
+  const int pm = g_pair_mode.load(std::memory_order_relaxed);
+  if (pm == 0 || (pm < 0 && (f <= kBM || h <= kBM)) || (T + kBK - 1) / kBK < 16) return false;
+  return mode == 1 || 2.0 * (double)f * (double)h * (double)T >= kWgradTransposeMinFlop;
+}
+
 int launch_check(cudaError_t e, const char* what) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -400,6 +421,26 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     rc = launch_check(e, "dropout backward");
     if (rc) return rc;
   }
+  // B3 and B4 reduce over the tokens, so both of their operands are MN-major as
+  // stored, and a GEMM with two MN-major operands runs about 5 % slower than one
+  // with a K-major operand (measured on the MT-NLG layer).  When dXacc is free (t == 1
+  // or the all-slices call) and the GEMMs are large, it holds transposed copies X^T
+  // and dZ^T ([h, tokens] bf16 each: together exactly dXacc's bytes), made by one
+  // launch after B1; B3 reads dZ^T and B4 X^T as K-major operands.  Same products,
+  // same reduction order per tile.
+  mlp_bf16* Xt = nullptr;
+  mlp_bf16* dZt = nullptr;
+  if (t == 1 && wgrad_transposed(h, f, tokens, dXacc)) {
+    Xt = reinterpret_cast<mlp_bf16*>(dXacc);
+    dZt = Xt + (int64_t)h * tokens;
+    const int ts = trace_pre(s);
+    const cudaError_t e =
+        launch_kernel(k_transpose_bf16, dim3((h + kTrTile - 1) / kTrTile, (unsigned)((tokens + kTrTile - 1) / kTrTile), 2),
+                      dim3(kTrThreads), 0, s, 1, 1, TransposeJob{X, Xt}, TransposeJob{dZ, dZt}, tokens, h);
+    trace_post(ts, s, kTraceTranspose, tokens, h, 0);
+    rc = launch_check(e, "transposed copies of X and dZ");
+    if (rc) return rc;
+  }
   const int i0 = slice < 0 ? 0 : slice;
   const int i1 = slice < 0 ? 1 : slice + 1;
   for (int i = i0; i < i1; ++i) {
@@ -443,14 +484,16 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
     e3.kind = accumulate ? kEpiF32Add : kEpiF32Store;
     e3.ld = h;
     e3.g_out = dB + c * h;
-    rc = gemm(st, Y + c, true, ffn, dZ, true, h, f, h, T, e3, s, kTraceB3, true);
+    rc = dZt ? gemm(st, Y + c, true, ffn, dZt, false, T, f, h, T, e3, s, kTraceB3, true)
+             : gemm(st, Y + c, true, ffn, dZ, true, h, f, h, T, e3, s, kTraceB3, true);
     if (rc) return rc;
     // B4: dA_i (+)= X^T dU_i                             (M = h, N = f, K = T)
     EpiParams e4{};
     e4.kind = accumulate ? kEpiF32Add : kEpiF32Store;
     e4.ld = ffn;
     e4.g_out = dA + c;
-    rc = gemm(st, X, true, h, dU + c, true, ffn, h, f, T, e4, s, kTraceB4, true);
+    rc = Xt ? gemm(st, Xt, false, T, dU + c, true, ffn, h, f, T, e4, s, kTraceB4, true)
+            : gemm(st, X, true, h, dU + c, true, ffn, h, f, T, e4, s, kTraceB4, true);
     if (rc) return rc;
   }
   return MLP_OK;
@@ -922,6 +965,12 @@ int mlp_set_attn_fused(int enable) {
 int mlp_set_tile_scheduler(int mode) {
   if (mode < -1 || mode > 1) return fail(MLP_EINVAL, "mlp_set_tile_scheduler: %d not in {-1, 0, 1}", mode);
   g_tile_sched.store(mode, std::memory_order_relaxed);
+  return MLP_OK;
+}
+
+int mlp_set_wgrad_transpose(int mode) {
+  if (mode < -1 || mode > 1) return fail(MLP_EINVAL, "mlp_set_wgrad_transpose: %d not in {-1, 0, 1}", mode);
+  g_wgrad_transpose.store(mode, std::memory_order_relaxed);
   return MLP_OK;
 }
 

@@ -247,6 +247,11 @@ int gemm(DeviceState* st, const void* a, bool a_mn, int64_t lda, const void* b, 
   if (!a_mn && !b_mn) return GB_LAUNCH(false, false);
   if (a_mn && b_mn) return GB_LAUNCH(true, true);
 #undef GB_LAUNCH
+  // (MN, K): only the weight-gradient product dB = Y^T dZ with a transposed copy of
+  // dZ (mlp_bwd), which always runs on CTA pairs with a deep enough reduction
+  if (a_mn && !b_mn && pair && !wide)
+    return launch_gemm_t<true, false, true, false, false>(st, mA, mB, mC, mO0, mO1, M, N, K, ep, raster_n_fast, group,
+                                                          l2_hints, stream, trace_kind, 1, 1, kCausalNone, late_wait);
   return fail(MLP_EUNSUPPORTED, "operand layout combination not instantiated");
 }
 

@@ -44,6 +44,7 @@ _SIGNATURES = {
     "mlp_set_dependent_launch": (_i32, [_i32]),
     "mlp_set_split_tail": (_i32, [_i32]),
     "mlp_set_tile_scheduler": (_i32, [_i32]),
+    "mlp_set_wgrad_transpose": (_i32, [_i32]),
     "mlp_set_attn_fused": (_i32, [_i32]),
     "adam_step": (_i32, [_i64, _vp, _f32, _vp, _vp, _vp, _vp, _f32, _f32, _f32, _f32, _f32, _i32, _vp]),
     "attn_fwd": (_i32, [_i32, _i32, _i32, _i64, _i32, _f32, _u64, _u64] + [_vp] * 11 + [_vp]),
@@ -234,9 +235,16 @@ def mlp_set_tile_scheduler(mode: int):
     _check(load().mlp_set_tile_scheduler(int(mode)))
 
 
+def mlp_set_wgrad_transpose(mode: int):
+    """1 the weight-gradient GEMMs read transposed copies of X and dZ (held in dXacc)
+    whenever they can, 0 never, -1 (default) when the GEMMs are large enough."""
+    _check(load().mlp_set_wgrad_transpose(int(mode)))
+
+
 TRACE_NAMES = {0: "F1 gemm X.A_i +a, GeLU", 1: "F2 gemm Y_i.B_i (+dropout,+residual)", 2: "B2 gemm dZ.B_i^T *GeLU'",
                3: "B3 gemm Y_i^T.dZ (+= dB)", 4: "B4 gemm X^T.dU_i (+= dA)", 5: "B5 gemm dU_i.A_i^T (+dO)",
                10: "dropout backward + db", 11: "column sum da", 12: "accumulator reset", 14: "adam step",
+               15: "transposed copies X^T, dZ^T",
                20: "attention GEMM", 21: "softmax, softmax-grad row sums", 22: "fused attention core"}
 GEMM_KINDS = (0, 1, 2, 3, 4, 5)
 
@@ -308,7 +316,9 @@ class BlockBuffers:
         self.dU = torch.empty(tokens, ffn, **bf)
         self.dX = torch.empty(tokens, h, **bf)
         self.Zacc = torch.empty(tokens, h, **f32) if t > 1 else None
-        self.dXacc = torch.empty(tokens, h, **f32) if t > 1 else None
+        # the one-slice calls' sum over slices; otherwise scratch for the transposed
+        # operands of the weight-gradient GEMMs
+        self.dXacc = torch.empty(tokens, h, **f32)
         if grads is None:
             grads = (torch.zeros(h, ffn, **f32), torch.zeros(ffn, **f32), torch.zeros(ffn, h, **f32),
                      torch.zeros(h, **f32))
