@@ -435,6 +435,7 @@ def run_ours(args, wl, rank, world, dist):
     gb_build.build()
     mlp.load()
     mlp.mlp_set_tile_scheduler({"default": -1, "static": 0, "dynamic": 1}[args.tile_scheduler])
+    mlp.mlp_set_wgrad_transpose({"default": -1, "off": 0, "on": 1}[args.wgrad_transpose])
     if args.attn_only:
         # the attention block alone (the next row), e.g. for a counter capture of its kernels
         out = attn_bench(wl, dev, torch.cuda.current_stream(dev), args)
@@ -712,6 +713,7 @@ def run_ours(args, wl, rank, world, dist):
         "pct_of_nominal_peak": 100.0 * value / (world * NOMINAL_BF16_DENSE_TFLOPS),
         "config": workload_config(wl, args.slice_mode, world),
         "run": {"tile_order": args.tile_scheduler,
+                "wgrad_transposed_operands": args.wgrad_transpose,
                 "grad_init": ("grad_accum_reset + every micro-batch adds (inside the timed region)"
                               if args.reset_each_step else
                               "first micro-batch of each step writes dA/da/dB/db, later ones add; no reset pass")},
@@ -753,6 +755,9 @@ def main():
     ap.add_argument("--tile-scheduler", default="default", choices=["default", "dynamic", "static"],
                     help="order in which the GEMMs hand out output tiles (results are bit-identical): "
                          "default = dynamic for the batched attention products only")
+    ap.add_argument("--wgrad-transpose", default="default", choices=["default", "on", "off"],
+                    help="whether the weight-gradient GEMMs read transposed copies of X and dZ (bit-identical "
+                         "results): default = for GEMMs of 1e12 FLOP or more")
     ap.add_argument("--no-accumulate-form", action="store_true",
                     help="skip timing the += form (reset outside the timed region, every micro-batch adds)")
     ap.add_argument("--reset-each-step", action="store_true",
