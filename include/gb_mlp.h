@@ -193,7 +193,8 @@ int attn_fwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
  * rowsum(dP P) is taken as rowsum(dO * O), the same quantity (P V = O), and dP is
  * never stored: the product dO V^T goes straight into dS in the GEMM's epilogue.
  * dZ, dO [tokens, h] and dS (P's shape) are bf16 workspaces (dS is written only in
- * the tiles on or below the causal diagonal that are read back),
+ * the tiles on or below the causal diagonal that are read back, and may also hold
+ * transposed copies of dZ and X, see mlp_set_wgrad_transpose),
  * dP an fp32 workspace of at least n_seq * nh * seq_len floats (the row sums),
  * dQKV [tokens, 3h] bf16, dX [tokens, h] bf16.  Returns MLP_OK or an error.
  */
@@ -281,6 +282,9 @@ int mlp_set_split_tail(int enable);
  *  -1  (the default) the same, for GEMMs of at least 1e12 FLOP each (smaller ones
  *      do not repay the copies);
  *   0  never.
+ * attn_bwd does the same for dWo (+)= O^T dZ and dWqkv (+)= X^T dQKV when seq_len
+ * >= the head size: the copies dZ^T and X^T go to its dS workspace, which is free
+ * before the attention core writes it and after the products read it.
  * The products and their reduction order are the same either way.  Returns
  * MLP_OK or MLP_EINVAL.
  */

@@ -249,6 +249,39 @@ def test_attention_tile_scheduler_changes_no_bit():
             assert torch.equal(r[n], res[0][n]), n
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "unfused"])
+def test_attention_wgrad_transposed_operands_change_no_bit(fused):
+    """dWo and dWqkv reading transposed copies of dZ and X (K-major operands held in
+    the dS workspace, before the core writes it and after the products read it)
+    give, bit for bit, what they give reading dZ and X as MN-major operands; with
+    either attention core.  The copies run only when asked for."""
+    T, h, nh, t, L = 2048, 2048, 16, 8, 1024
+    gen = torch.Generator().manual_seed(6)
+    w = tuple(x.cuda() for x in _weights(h, gen, std=0.5 / np.sqrt(h)))
+    X = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
+    dOut = torch.randn(T, h, generator=gen).to(torch.bfloat16).cuda()
+    res = []
+    try:
+        mlp.mlp_set_attn_fused(fused)
+        for mode in (0, 1):
+            mlp.mlp_set_wgrad_transpose(mode)
+            buf = mlp.AttnBuffers(T, h, nh, L)
+            tr = mlp.Trace(capacity=64)
+            tr.start()
+            mlp.attn_step(h, nh, t, L, 0.1, 1234, w, X, dOut, buf, accumulate=False)
+            torch.cuda.synchronize()
+            tr.stop()
+            assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
+            copies = sum(1 for kind, _, _ in tr.entries if kind == 15)
+            assert copies == (2 if mode == 1 else 0), (mode, copies)
+            res.append({n: getattr(buf, n).clone() for n in ("out", "dQKV", "dX", "dWqkv", "dbqkv", "dWo", "dbo")})
+    finally:
+        mlp.mlp_set_wgrad_transpose(-1)
+        mlp.mlp_set_attn_fused(True)
+    for n in res[0]:
+        assert torch.equal(res[1][n], res[0][n]), n
+
+
 @pytest.mark.parametrize("T,h,nh,L", [
     (2048, 2048, 16, 1024),   # d = 128, two sequences
     (1088, 640, 4, 136),      # d = 160 (three 64-column atoms, the last half used), ragged 136-token sequences

@@ -291,19 +291,20 @@ std::atomic<int> g_wgrad_transpose{-1};
 // 0.27 TFLOP weight-gradient GEMMs: 6 us saved, 14 us of copies).
 constexpr double kWgradTransposeMinFlop = 1e12;
 
-// Whether mlp_bwd's all-slices call gives B3 and B4 one K-major operand each
-// through transposed copies of dZ and X held in dXacc: the switch allows it, dXacc
-// is there and 16-byte aligned, the token count suits the copies and the tensor
-// maps (a multiple of 8), and both GEMMs take the CTA-pair form with a reduction of
-// 16 k-blocks or more (the forms the (K, MN) and (MN, K) launches instantiate);
-// by default, only GEMMs large enough to repay the copies.
-bool wgrad_transposed(int h, int f, int64_t T, const float* dXacc) {
+// Whether a weight-gradient GEMM D[M, N] (+)= A^T B, reducing over T tokens, may
+// read a transposed copy of one operand as a K-major operand: the switch allows
+// it, the scratch for the copy is there and 16-byte aligned, the token count
+// suits the copy kernel and the tensor maps (a multiple of 8), and the GEMM takes
+// the CTA-pair form with a reduction of 16 k-blocks or more (the forms the
+// (K, MN) and (MN, K) launches instantiate); by default, only GEMMs large enough
+// to repay the copy.
+bool wgrad_transposed(int M, int N, int64_t T, const void* scratch) {
   const int mode = g_wgrad_transpose.load(std::memory_order_relaxed);
-  if (mode == 0 || dXacc == nullptr || (reinterpret_cast<uintptr_t>(dXacc) & 15) != 0) return false;
+  if (mode == 0 || scratch == nullptr || (reinterpret_cast<uintptr_t>(scratch) & 15) != 0) return false;
   if (T % 8 != 0 || (T + kTrTile - 1) / kTrTile > 65535) return false;
   const int pm = g_pair_mode.load(std::memory_order_relaxed);
-  if (pm == 0 || (pm < 0 && (f <= kBM || h <= kBM)) || (T + kBK - 1) / kBK < 16) return false;
-  return mode == 1 || 2.0 * (double)f * (double)h * (double)T >= kWgradTransposeMinFlop;
+  if (pm == 0 || (pm < 0 && M <= kBM) || (T + kBK - 1) / kBK < 16) return false;
+  return mode == 1 || 2.0 * (double)M * (double)N * (double)T >= kWgradTransposeMinFlop;
 }
 
 int launch_check(cudaError_t e, const char* what) {
@@ -311,6 +312,18 @@ int launch_check(cudaError_t e, const char* what) {
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return fail(MLP_ECUDA, "%s launch: %s", what, cudaGetErrorString(e));
   return MLP_OK;
+}
+
+// One launch of k_transpose_bf16 for one or two [rows, cols] matrices (j1.in may
+// be null), traced as kTraceTranspose.
+int launch_transposes(cudaStream_t s, int64_t rows, int cols, TransposeJob j0, TransposeJob j1, const char* what) {
+  const unsigned jobs = j1.in != nullptr ? 2u : 1u;
+  const int ts = trace_pre(s);
+  const cudaError_t e = launch_kernel(k_transpose_bf16, dim3((cols + kTrTile - 1) / kTrTile,
+                                                             (unsigned)((rows + kTrTile - 1) / kTrTile), jobs),
+                                      dim3(kTrThreads), 0, s, 1, 1, j0, j1, rows, cols);
+  trace_post(ts, s, kTraceTranspose, rows, cols, 0);
+  return launch_check(e, what);
 }
 
 template <int CHUNKS>
@@ -430,15 +443,10 @@ int mlp_bwd(int h, int ffn, int t, int slice, int64_t tokens, float p, uint64_t 
   // same reduction order per tile.
   mlp_bf16* Xt = nullptr;
   mlp_bf16* dZt = nullptr;
-  if (t == 1 && wgrad_transposed(h, f, tokens, dXacc)) {
+  if (t == 1 && wgrad_transposed(f, h, tokens, dXacc) && wgrad_transposed(h, f, tokens, dXacc)) {
     Xt = reinterpret_cast<mlp_bf16*>(dXacc);
     dZt = Xt + (int64_t)h * tokens;
-    const int ts = trace_pre(s);
-    const cudaError_t e =
-        launch_kernel(k_transpose_bf16, dim3((h + kTrTile - 1) / kTrTile, (unsigned)((tokens + kTrTile - 1) / kTrTile), 2),
-                      dim3(kTrThreads), 0, s, 1, 1, TransposeJob{X, Xt}, TransposeJob{dZ, dZt}, tokens, h);
-    trace_post(ts, s, kTraceTranspose, tokens, h, 0);
-    rc = launch_check(e, "transposed copies of X and dZ");
+    rc = launch_transposes(s, tokens, h, TransposeJob{X, Xt}, TransposeJob{dZ, dZt}, "transposed copies of X and dZ");
     if (rc) return rc;
   }
   const int i0 = slice < 0 ? 0 : slice;
@@ -790,12 +798,22 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
     rc = launch_check(e, "dropout backward");
     if (rc) return rc;
   }
-  // dWo (+)= O^T dZ
+  // dWo (+)= O^T dZ.  Both operands are MN-major as stored (the reduction runs over
+  // the tokens); as for mlp_bwd's B3, a large enough GEMM reads a transposed copy
+  // dZ^T instead, held in the dS workspace, which is free until the attention core
+  // writes it (dS holds ns nh L L >= tokens h elements when L >= d).
+  const bool ds_holds_copy = L >= d;
   EpiParams ew{};
   ew.kind = acc ? kEpiF32Add : kEpiF32Store;
   ew.ld = h;
   ew.g_out = dWo;
-  rc = gemm(st, O, true, h, dZ, true, h, h, h, T, ew, s, kTraceAttnGemm);
+  if (ds_holds_copy && wgrad_transposed(h, h, tokens, dS)) {
+    rc = launch_transposes(s, tokens, h, TransposeJob{dZ, dS}, TransposeJob{nullptr, nullptr}, "transposed copy of dZ");
+    if (rc) return rc;
+    rc = gemm(st, O, true, h, dS, false, T, h, h, T, ew, s, kTraceAttnGemm);
+  } else {
+    rc = gemm(st, O, true, h, dZ, true, h, h, h, T, ew, s, kTraceAttnGemm);
+  }
   if (rc) return rc;
   // dO = dZ Wo^T
   EpiParams ed{};
@@ -872,11 +890,19 @@ int attn_bwd(int h, int nh, int t, int64_t tokens, int seq_len, float p, uint64_
     rc = launch_check(e, "bias-gradient column sum");
     if (rc) return rc;
   }
+  // dWqkv reads a transposed copy X^T (K-major) when large enough, in the dS
+  // workspace again: every product that reads dS precedes it on the stream
   EpiParams eq{};
   eq.kind = acc ? kEpiF32Add : kEpiF32Store;
   eq.ld = h3;
   eq.g_out = dWqkv;
-  rc = gemm(st, X, true, h, dQKV, true, h3, h, (int)h3, T, eq, s, kTraceAttnGemm);
+  if (ds_holds_copy && wgrad_transposed(h, (int)h3, tokens, dS)) {
+    rc = launch_transposes(s, tokens, h, TransposeJob{X, dS}, TransposeJob{nullptr, nullptr}, "transposed copy of X");
+    if (rc) return rc;
+    rc = gemm(st, dS, false, T, dQKV, true, h3, h, (int)h3, T, eq, s, kTraceAttnGemm);
+  } else {
+    rc = gemm(st, X, true, h, dQKV, true, h3, h, (int)h3, T, eq, s, kTraceAttnGemm);
+  }
   if (rc) return rc;
   EpiParams ex{};
   ex.kind = kEpiResAdd;
