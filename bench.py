@@ -96,7 +96,8 @@ def hbm_kernel_rooflines(trace, wl, peaks, reset_ms):
     summ = trace.summary()
     out = {}
     spec = {10: ("dropout backward + db (B1)", 4 * T * h + 4 * h),
-            11: ("column sum da", 2 * T * F + 4 * F)}
+            11: ("column sum da", 2 * T * F + 4 * F),
+            15: ("transposed copies of X and dZ for B3/B4", 8 * T * h)}
     for kind, (name, nbytes) in spec.items():
         if kind in summ and summ[kind][0] > 0:
             ms = summ[kind][1] / summ[kind][0]
