@@ -42,10 +42,24 @@ def test_small_workload_full_parity():
     compare_full(s, g_outs, g_grads, r_outs, r_grads, label="small")
 
 
-def _sampled_check(wl, slice_mode, n_rows=24, n_entries=96, seed=0, first_overwrites=False):
+def _full_da(Xs, dZs, A, a, B, ffn, block=4096):
+    """All of da from the oracle: the column sums of every micro-batch's dU, a
+    block of columns at a time (so that only slice-sized blocks of A and B are
+    decoded to float64)."""
+    out = np.zeros(ffn)
+    for c0 in range(0, ffn, block):
+        cols = np.arange(c0, min(ffn, c0 + block))
+        for X, dZ in zip(Xs, dZs):
+            out[cols] += orc.columns_dU(cols, X, A, a, B, dZ, mirror=True).sum(axis=0)
+    return out
+
+
+def _sampled_check(wl, slice_mode, n_rows=64, n_entries=256, seed=0, first_overwrites=False, full_da=True):
     """Runs the workload on the GPU (inputs drawn on the GPU with the seeded
-    generators) and checks sampled outputs against the oracle.  first_overwrites:
-    no reset; the first micro-batch overwrites the accumulators (which start as
+    generators) and checks against the oracle: n_rows token rows of U, Y, O, dU
+    and dX, the whole of dZ and db, n_entries entries each of dA and dB, and all
+    of da (full_da; else da at the sampled dA columns).  first_overwrites: no
+    reset; the first micro-batch overwrites the accumulators (which start as
     NaN), as the benchmark runs it."""
     dev = torch.device("cuda")
     w = gin.make_weights(wl.h, wl.ffn, device=dev)
@@ -102,9 +116,13 @@ def _sampled_check(wl, slice_mode, n_rows=24, n_entries=96, seed=0, first_overwr
     cA = np.concatenate([[0, F - 1], rng.integers(0, F, n_entries - 2)])
     ref_dA = sum(orc.wgrad_dA_entries(rA, cA, Xs[j], A, a, B, dZs[j], mirror=True) for j in range(wl.k))
     got_dA = to_f64(buf.dA[torch.from_numpy(rA).to(dev), torch.from_numpy(cA).to(dev)])
-    ca = np.unique(cA)
-    ref_da = sum(orc.columns_dU(ca, Xs[j], A, a, B, dZs[j], mirror=True).sum(axis=0) for j in range(wl.k))
-    got_da = to_f64(buf.da[torch.from_numpy(ca).to(dev)])
+    if full_da:
+        ref_da = _full_da(Xs, dZs, A, a, B, F)
+        got_da = to_f64(buf.da)
+    else:
+        ca = np.unique(cA)
+        ref_da = sum(orc.columns_dU(ca, Xs[j], A, a, B, dZs[j], mirror=True).sum(axis=0) for j in range(wl.k))
+        got_da = to_f64(buf.da[torch.from_numpy(ca).to(dev)])
     # the relative-to-max bar, with the max taken over the sampled reference entries
     errs["dB"] = rel_err(got_dB, ref_dB)
     errs["dA"] = rel_err(got_dA, ref_dA)
@@ -122,17 +140,20 @@ def test_mid_workload_sampled_parity():
 def test_mtnlg_layer_sampled_parity():
     """2048 tokens, h 20480, ffn 81920, t 8: all slices per call, the first (only)
     micro-batch writing the gradients, as benchmarked."""
-    _sampled_check(gin.WORKLOADS["mtnlg"], "all", n_rows=16, n_entries=64, first_overwrites=True)
+    _sampled_check(gin.WORKLOADS["mtnlg"], "all", first_overwrites=True)
 
 
 def test_mtnlg_layer_one_slice_calls_sampled_parity():
     """The MT-NLG layer with its eight slices as eight calls in turn (fp32 partial
     sums in HBM)."""
-    _sampled_check(gin.WORKLOADS["mtnlg"], "each", n_rows=8, n_entries=32, seed=1)
+    _sampled_check(gin.WORKLOADS["mtnlg"], "each", seed=1)
 
 
 @pytest.mark.parametrize("name,first_overwrites", [("sweep1", True), ("sweep4", False), ("sweep16", True),
                                                    ("sweep32", False)])
 def test_accumulation_sweep_sampled_parity(name, first_overwrites):
-    """h 8192, ffn 32768, t 4, one slice per call in turn, micro-batches accumulated."""
-    _sampled_check(gin.WORKLOADS[name], "each", n_rows=12, n_entries=48, first_overwrites=first_overwrites)
+    """h 8192, ffn 32768, t 4, one slice per call in turn, micro-batches accumulated.
+    All of da is checked up to 4 micro-batches; at 16 and 32 (35 and 70 TFLOP of
+    float64 host work for it) at the 256 sampled dA columns."""
+    wl = gin.WORKLOADS[name]
+    _sampled_check(wl, "each", first_overwrites=first_overwrites, full_da=wl.k <= 4)
