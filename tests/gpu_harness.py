@@ -42,11 +42,12 @@ class Shape:
 
 
 def run_gpu(shape, weights_dev, microbatches_dev, slice_mode="all", keep_all=False, buf=None, reset=True,
-            first_overwrites=False):
+            first_overwrites=False, token_offset0=0):
     """Forward+backward of every micro-batch on the GPU; gradients accumulate.
 
     reset: zero the accumulators first (grad_accum_reset); first_overwrites: the
     first micro-batch overwrites them instead (accumulate = 0), later ones add.
+    Micro-batch j runs at token offset token_offset0 + j * tokens.
     Returns (per-micro-batch outputs, gradients) as CPU tensors."""
     T = microbatches_dev[0][0].shape[0]
     if buf is None:
@@ -55,7 +56,7 @@ def run_gpu(shape, weights_dev, microbatches_dev, slice_mode="all", keep_all=Fal
         mlp.grad_accum_reset(shape.h, shape.ffn, buf.dA, buf.da, buf.dB, buf.db)
     outs = []
     for j, (X, dO) in enumerate(microbatches_dev):
-        mlp.block_step(shape, weights_dev, X, dO, buf, token_offset=j * T, slice_mode=slice_mode,
+        mlp.block_step(shape, weights_dev, X, dO, buf, token_offset=token_offset0 + j * T, slice_mode=slice_mode,
                        accumulate=not (first_overwrites and j == 0))
         if keep_all or j == len(microbatches_dev) - 1:
             outs.append({k: getattr(buf, k).cpu() for k in ("U", "Y", "O", "dZ", "dU", "dX")})

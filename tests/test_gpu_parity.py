@@ -185,6 +185,39 @@ def test_first_microbatch_overwrite_equals_reset_then_accumulate(mode):
         assert rel_err(to_f64(g_new[k]), r_grads[k]) <= F32_TOL, k
 
 
+@pytest.mark.parametrize("mode", ["all", "each"])
+def test_accumulation_invariance_and_sum_of_singles(mode):
+    """Gradient accumulation (MT-NLG summary page, Key points): k micro-batches of
+    T tokens accumulated with token offsets j T give the gradients of one batch of
+    k T tokens at offset 0, up to fp32 summation order (1e-3, relative to max), with
+    the same dropout mask, so every output row is bit-identical; and they equal
+    the sum, in float64, of the k micro-batches' gradients computed one at a time,
+    up to the fp32 rounding of the running sum (1e-6)."""
+    s = Shape(tokens=256, h=256, ffn=1024, t=2, k=3)
+    w_dev, mbs_dev, _, _ = make_case(s)
+    outs_acc, g_acc = run_gpu(s, w_dev, mbs_dev, slice_mode=mode, keep_all=True)
+    # one batch of k T tokens
+    Xc = torch.cat([X for X, _ in mbs_dev])
+    dOc = torch.cat([dO for _, dO in mbs_dev])
+    sc = Shape(tokens=s.k * s.tokens, h=s.h, ffn=s.ffn, t=s.t, k=1)
+    outs_cat, g_cat = run_gpu(sc, w_dev, [(Xc, dOc)], slice_mode=mode)
+    for key in ("U", "Y", "O", "dZ", "dU", "dX"):
+        got = torch.cat([outs_acc[j][key] for j in range(s.k)])
+        assert torch.equal(got, outs_cat[0][key]), key
+    for key in g_acc:
+        e = rel_err(to_f64(g_acc[key]), to_f64(g_cat[key]))
+        assert e <= F32_TOL, (key, e)
+    # the sum of single micro-batches
+    singles = {key: 0.0 for key in g_acc}
+    for j in range(s.k):
+        _, g_j = run_gpu(s, w_dev, [mbs_dev[j]], slice_mode=mode, first_overwrites=True, token_offset0=j * s.tokens)
+        for key in singles:
+            singles[key] = singles[key] + to_f64(g_j[key])
+    for key in g_acc:
+        e = rel_err(to_f64(g_acc[key]), singles[key])
+        assert e <= 1e-6, (key, e)
+
+
 def test_bounded_wait_reports_timeout():
     assert mlp.mlp_sync_status() == mlp.MLP_OK
     mlp.mlp_wait_timeout_probe(1000000)   # 1 ms

@@ -42,6 +42,18 @@ def test_small_workload_full_parity():
     compare_full(s, g_outs, g_grads, r_outs, r_grads, label="small")
 
 
+def test_mid_workload_full_parity():
+    """2048 tokens, h 4096, ffn 16384, t 1, four accumulated micro-batches, against
+    the whole oracle (6.6 TFLOP of float64 host work): every element of the last
+    micro-batch's U, Y, O, dZ, dU, dX and of the accumulated dA, da, dB, db."""
+    wl = gin.WORKLOADS["mid"]
+    s = Shape(wl.tokens, wl.h, wl.ffn, wl.t, wl.k, wl.p, wl.seed)
+    w_dev, mbs_dev, w64, mbs64 = make_case(s)
+    g_outs, g_grads = run_gpu(s, w_dev, mbs_dev)
+    r_outs, r_grads = run_oracle(s, w64, mbs64, mirror=True)
+    compare_full(s, g_outs, g_grads, r_outs, r_grads, label="mid")
+
+
 def _full_da(Xs, dZs, A, a, B, ffn, block=4096):
     """All of da from the oracle: the column sums of every micro-batch's dU, a
     block of columns at a time (so that only slice-sized blocks of A and B are
