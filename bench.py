@@ -243,7 +243,26 @@ def workload_config(wl, slice_mode, world):
                   % (4 * wl.h * wl.ffn / 1e9, 8 * wl.h * wl.ffn / 1e9)}
 
 
-def other_workloads(dev, stream, steps=5, warmup=2):
+def oracle_workload_time(wl, n_mb):
+    """The whole oracle (float64 numpy on the host cores), forward + backward of the
+    first n_mb micro-batches of a workload over all its slices, gradients summed:
+    the CPU baseline of the smaller workloads."""
+    from oracle import mlp_oracle as orc
+    from transformer_lm_megatron_gb300 import inputs as gin
+    dec = lambda t: orc.bf16_to_f64(gin.bf16_bits(t))  # noqa: E731
+    A, a, B, b = (dec(x) for x in gin.make_weights(wl.h, wl.ffn))
+    mbs = [tuple(dec(x) for x in gin.make_microbatch(wl.tokens, wl.h, j)) for j in range(n_mb)]
+    t0 = time.perf_counter()
+    for j, (X, dO) in enumerate(mbs):
+        fw = orc.mlp_fwd(X, A, a, B, b, wl.t, wl.p, wl.seed, token_offset=j * wl.tokens, mirror=True)
+        orc.mlp_bwd(dO, X, A, B, fw["U"], fw["Y"], fw["keep"], wl.t, wl.p, mirror=True)
+    dt = time.perf_counter() - t0
+    flops = 12 * wl.tokens * wl.h * wl.ffn * n_mb
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": _cpu_cores(), "kind": "oracle",
+            "sample": f"{n_mb} of {wl.k} micro-batches, all {wl.t} slices, fwd+bwd, float64 numpy, {dt:.1f} s"}
+
+
+def other_workloads(dev, stream, steps=5, warmup=2, cpu_oracle=True):
     """fwd+bwd TFLOP/s of the smaller named workloads, each step being all of its
     micro-batches (the first writes the gradients, the rest add).  The sweep runs
     one slice per call, as its workload description says; the others all slices
@@ -298,6 +317,10 @@ def other_workloads(dev, stream, steps=5, warmup=2):
                      "slice_calls": mode, "ms_per_step": ms, "TFLOPs": w.flops_total() / (ms / 1e3) / 1e12,
                      "graph_ms_per_step": gms, "graph_TFLOPs": w.flops_total() / (gms / 1e3) / 1e12}
         del weights, mbs, buf
+        # the whole oracle on the host cores: every micro-batch of tiny and small, one of mid
+        n_mb = {"tiny": w.k, "small": w.k, "mid": 1}.get(name)
+        if cpu_oracle and n_mb:
+            out[name]["cpu_oracle"] = oracle_workload_time(w, n_mb)
     if mlp.mlp_sync_status(stream) != mlp.MLP_OK:
         raise RuntimeError(mlp.last_error())
     return out
@@ -650,7 +673,7 @@ def run_ours(args, wl, rank, world, dist):
     # ---- the other named workloads (secondary figures; the headline is the MT-NLG layer)
     others = None
     if not args.no_others and wl.name == "mtnlg":
-        others = other_workloads(dev, stream)
+        others = other_workloads(dev, stream, cpu_oracle=(rank == 0 and world == 1 and not args.no_cpu_baseline))
 
     # ---- next row: the tensor-sliced self-attention block at the MT-NLG layer
     # shape (h 20480, 128 heads, t 8, one 2048-token sequence), forward + backward
