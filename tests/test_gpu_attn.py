@@ -158,7 +158,7 @@ def test_attention_block_mtnlg_shape_sampled_parity():
     assert mlp.mlp_sync_status() == mlp.MLP_OK, mlp.last_error()
 
     rng = np.random.default_rng(11)
-    rows = np.unique(np.concatenate([[0, 1, 127, 128, 1023, T - 1], rng.integers(0, T, 4)]))
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 1023, T - 1], rng.integers(0, T, 58)]))
     heads = [0, 61, nh - 1]
     n_e = 256
     rq = np.concatenate([[0, h - 1], rng.integers(0, h, n_e - 2)])
